@@ -1,0 +1,187 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged-KV grouped-query attention library.
+ *
+ * Operations (cited by page title and section):
+ *   - decode, split-KV: "vllm/attention/ops/triton_decode_attention.py",
+ *     _fwd_grouped_kernel_stage1 (per-split partial output and log-sum-exp)
+ *     and _fwd_kernel_stage2 (merge of the splits by LSE);
+ *   - prefix-prefill / extend: "vllm/attention/ops/prefix_prefill.py",
+ *     context_attention_fwd / _fwd_kernel (new queries see the cached context
+ *     unmasked and the new tokens causally);
+ *   - sinks, window_left, fp8 descales, plan/bind/run split and the
+ *     caller-owned scratch workspace: "vllm/v1/attention/backends/b12x",
+ *     B12xPagedAttentionImpl (__init__, forward, _prepare_fp8_descales).
+ *
+ * What every call computes, for request b, query row at sequence position
+ * pos_q, q head h and kv head g = h / (Hq / Hkv):
+ *   J      = { j : 0 <= j <= pos_q, and (window <= 0 or pos_q - j < window) }
+ *   K_j    = k_cache[block_table[b][j / page_size]][j % page_size][g][:]
+ *   s_j    = scale * (q . K_j);  s_j = cap * tanh(s_j / cap) when soft_cap > 0
+ *   m      = max(max_J s_j, sink_h)            (sink only when sinks != NULL)
+ *   Z      = sum_J exp(s_j - m) + exp(sink_h - m)
+ *   out    = sum_J exp(s_j - m) V_j / Z        (bf16)
+ *   lse    = m + ln Z                          (fp32, natural log)
+ * Decode has one query per request at pos_q = seq_lens[b] - 1.  Extend packs
+ * the new queries of request b in rows [query_start_loc[b], query_start_loc[b+1]),
+ * row i of the request at pos_q = ctx_b + i with
+ * ctx_b = seq_lens[b] - (query_start_loc[b+1] - query_start_loc[b]); the new
+ * tokens' K/V must already be in the pages.
+ * fp8 KV: element value = bf16( float(e4m3) * k_scale ) (same for V with
+ * v_scale), as the prefix-prefill page dequantises.
+ *
+ * Conventions
+ *   - Pointers named "device" must be device memory of the current device;
+ *     the caller owns every buffer, including the scratch workspace.  No call
+ *     allocates device memory.
+ *   - Calls enqueue work on `stream` (a cudaStream_t, NULL = legacy default
+ *     stream) and return without synchronising.
+ *   - Strides are in ELEMENTS; the innermost (head_dim) dimension is
+ *     contiguous.  KV base pointers and the byte strides of pages, slots and
+ *     kv heads must be multiples of 16 bytes (they feed TMA tensor maps).
+ *   - Metadata (block_table, seq_lens, query_start_loc) is int32, in device
+ *     memory.  Block-table entries past ceil(seq_lens[b] / page_size) are
+ *     never read.
+ *   - Errors: no exceptions cross the ABI.  Argument errors return
+ *     PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED before anything is enqueued.
+ *     Kernels never trap: a bounded wait that expires sets an error word in
+ *     the scratch header, which pa_check reports as PA_ERR_DEVICE.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,       /* null pointer, negative size, inconsistent shape */
+  PA_ERR_UNSUPPORTED = 2,       /* valid but outside what the kernels implement */
+  PA_ERR_SCRATCH_TOO_SMALL = 3, /* scratch_bytes < plan->scratch_bytes */
+  PA_ERR_CUDA = 4,              /* a CUDA runtime/driver call failed */
+  PA_ERR_DEVICE = 5             /* a kernel reported an error in the scratch header */
+} pa_status;
+
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
+typedef enum { PA_MODE_DECODE = 0, PA_MODE_EXTEND = 1 } pa_mode;
+
+/* Static problem description (capacities, never live lengths, except for the
+ * optional host seq_lens hint given to pa_plan). */
+typedef struct {
+  int32_t mode;               /* pa_mode */
+  int32_t num_q_heads;        /* Hq; Hq % Hkv == 0 and Hq / Hkv <= 16 */
+  int32_t num_kv_heads;       /* Hkv */
+  int32_t head_dim;           /* D in {64, 128, 256} */
+  int32_t page_size;          /* ps in {16, 32, 64} */
+  int32_t kv_dtype;           /* pa_kv_dtype */
+  int32_t max_batch;          /* capacity: requests per call */
+  int32_t max_pages_per_seq;  /* capacity: block-table row width */
+  int32_t max_total_q;        /* extend: capacity of packed query rows */
+  int32_t window;             /* sliding window W; 0 = off */
+  int32_t has_sinks;          /* 1: calls pass a [Hq] fp32 sink logit array */
+  float soft_cap;             /* 0 = off; else s = cap * tanh(s / cap) */
+  int32_t num_splits;         /* decode: 0 = planner's choice, >0 = max KV splits per request */
+  int32_t num_sms;            /* SMs to plan for; 0 = query the current device */
+} pa_shape;
+
+/* Plan produced by pa_plan; plain data, may be copied.  Fields other than
+ * scratch_bytes are the planner's launch choices, exposed for inspection. */
+typedef struct {
+  pa_shape shape;
+  int32_t tile_tokens;        /* keys per pipeline stage */
+  int32_t split_tiles;        /* decode: stages per KV split (0 when num_splits is fixed) */
+  int32_t max_splits;         /* decode: largest split count a request can get */
+  int32_t stages;             /* pipeline depth per warp */
+  int32_t warps;              /* compute warps per CTA */
+  int32_t bt_cache;           /* block-table entries staged in shared memory per CTA */
+  int32_t smem_bytes;         /* dynamic shared memory per CTA */
+  int32_t grid[3];            /* main kernel grid */
+  int64_t scratch_bytes;      /* device scratch the calls need (>= 256) */
+  int32_t reserved[8];
+} pa_plan_t;
+
+/* Plan a decode or extend call from capacities.  host_seq_lens (host memory,
+ * `batch` entries, may be NULL) lets the decode planner size KV splits to the
+ * actual lengths; without it the plan assumes every request is at capacity.
+ * Pure host code: no CUDA call is made unless shape->num_sms == 0.
+ * Returns PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED for shapes it cannot run. */
+pa_status pa_plan(const pa_shape* shape, const int32_t* host_seq_lens, int32_t batch,
+                  pa_plan_t* plan);
+
+/* Split-KV paged decode: stage 1 (per-split partial output and LSE, written to
+ * the scratch workspace) followed by the LSE merge (final out / lse).
+ *   q            device bf16, [batch, Hq, D], strides q_stride_tok / q_stride_head
+ *   k_cache, v_cache  device, [num_pages, page_size, Hkv, D] bf16 or e4m3 bytes,
+ *                strides kv_stride_page / kv_stride_tok / kv_stride_head
+ *                (both caches share the strides; K and V may be the two halves
+ *                of one [num_pages, 2, page_size, Hkv*D] allocation)
+ *   block_table  device int32 [batch, bt_stride] (bt_stride >= pages used)
+ *   seq_lens     device int32 [batch]; keys per request (>= 0)
+ *   scale        softmax scale applied to q.K before the soft-cap
+ *   sinks        device fp32 [Hq] when plan->shape.has_sinks, else NULL
+ *   k_scale, v_scale  per-tensor fp8 scales (ignored for bf16 KV)
+ *   out          device bf16 [batch, Hq, D], strides out_stride_tok / out_stride_head
+ *   lse          device fp32 [batch, Hq] contiguous, or NULL
+ *   scratch      device, >= plan->scratch_bytes bytes, 256-byte aligned; its
+ *                first 256 bytes are the error header (zero it once with
+ *                pa_scratch_init).  Contents are overwritten by every call.
+ * Concurrent calls must not share a scratch buffer. */
+pa_status pa_decode(const pa_plan_t* plan,
+                    const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                    const void* k_cache, const void* v_cache,
+                    int64_t kv_stride_page, int64_t kv_stride_tok, int64_t kv_stride_head,
+                    int32_t num_pages,
+                    const int32_t* block_table, int64_t bt_stride,
+                    const int32_t* seq_lens, int32_t batch,
+                    float scale, const float* sinks, float k_scale, float v_scale,
+                    void* out, int64_t out_stride_tok, int64_t out_stride_head,
+                    float* lse,
+                    void* scratch, int64_t scratch_bytes, void* stream);
+
+/* Prefix-prefill / extend over the paged cache (all keys, cached and new,
+ * are read from the pages).
+ *   q               device bf16 [total_q, Hq, D] (strides as for decode)
+ *   seq_lens        device int32 [batch]: cached + new tokens per request
+ *   query_start_loc device int32 [batch + 1], query_start_loc[0] = 0,
+ *                   non-decreasing, query_start_loc[batch] = total_q
+ *   out             device bf16 [total_q, Hq, D]; lse device fp32 [total_q, Hq] or NULL
+ * A scheduler kernel builds the (request, kv head, query tile) work list in
+ * the scratch workspace from the device metadata, longest first; the
+ * attention kernel is persistent and takes items from that list.  total_q
+ * must not exceed plan->shape.max_total_q.  Other arguments as for pa_decode. */
+pa_status pa_extend(const pa_plan_t* plan,
+                    const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                    const void* k_cache, const void* v_cache,
+                    int64_t kv_stride_page, int64_t kv_stride_tok, int64_t kv_stride_head,
+                    int32_t num_pages,
+                    const int32_t* block_table, int64_t bt_stride,
+                    const int32_t* seq_lens, const int32_t* query_start_loc,
+                    int32_t batch, int32_t total_q,
+                    float scale, const float* sinks, float k_scale, float v_scale,
+                    void* out, int64_t out_stride_tok, int64_t out_stride_head,
+                    float* lse,
+                    void* scratch, int64_t scratch_bytes, void* stream);
+
+/* Zero the 256-byte error header at the start of a scratch buffer (enqueued
+ * on `stream`).  Call once after allocating the scratch. */
+pa_status pa_scratch_init(void* scratch, void* stream);
+
+/* Synchronise `stream`, read and clear the scratch error header.  Returns
+ * PA_OK, PA_ERR_DEVICE (a kernel's bounded wait expired; the header's code is
+ * stored in *device_code when non-NULL) or PA_ERR_CUDA. */
+pa_status pa_check(void* scratch, void* stream, uint32_t* device_code);
+
+/* Static string for a status code. */
+const char* pa_status_string(pa_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -1,0 +1,612 @@
+// Split-KV paged decode for sm_103a.
+//
+// Operation: "vllm/attention/ops/triton_decode_attention.py",
+// _fwd_grouped_kernel_stage1 (one partial softmax-attention result plus its
+// log-sum-exp per KV split of each request and kv head) and _fwd_kernel_stage2
+// (merge of the splits by LSE).  Sinks follow "vllm/v1/attention/backends/b12x"
+// (attention_sink_bias, one fp32 logit per q head in the softmax denominator).
+//
+// Design (GB300): the KV stream is read once from HBM, so the kernel is built
+// around bytes in flight, not arithmetic.
+//   * One CTA = one (split, kv head, request) work item, 4 compute warps.
+//     Warp w takes tiles w, w+4, w+8, ... of the split, each tile being
+//     TS consecutive keys; every warp owns a private ring of NS stages that
+//     its lane 0 refills with TMA tensor loads straight out of the pages
+//     (page id from a block-table slice staged in shared memory).  No
+//     producer warp, no cross-warp barrier in the main loop.
+//   * The G q heads that share a kv head form the N dimension of warp-level
+//     bf16 MMAs: S^T = K Q^T (M = 16 keys, N = 8 heads) and
+//     O^T += V^T P^T (M = 16 dims, N = 8 heads), so a K/V element fetched
+//     once serves all G heads, and the 8-wide N keeps G = 8 free of padding.
+//     P^T is formed in registers with movmatrix.
+//   * fp8-e4m3 K/V are dequantised in registers to bf16 exactly as the
+//     prefix-prefill page does: bf16(float(code) * scale).
+//   * Online softmax in the log2 domain; per-thread partial row sums are
+//     reduced once at the end; the 4 warps' states are merged in shared
+//     memory.  A request with one split writes the final output directly;
+//     otherwise the merge kernel combines the splits.
+#include <cfloat>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Attended keys of request b and their split partition.  Splits are
+// tile-aligned; split boundaries are a free choice because the LSE merge is
+// an exact re-association of the same softmax sum.
+struct SplitRange {
+  int lo, hi;            // attended keys [lo, hi)
+  int tile0;             // first tile (tile t covers keys [t*TS, (t+1)*TS))
+  int n_tiles;
+  int tiles_per_split;
+  int n_splits;
+};
+
+__device__ __forceinline__ SplitRange split_range(const DecodeParams& p, int L) {
+  SplitRange r;
+  r.hi = L;
+  // sliding window: decode query at pos L-1 keeps key j iff (L-1) - j < W
+  r.lo = (p.window > 0) ? max(0, L - p.window) : 0;
+  const int ts = p.tile_tokens;
+  if (r.hi <= r.lo) {
+    r.tile0 = 0;
+    r.n_tiles = 0;
+    r.tiles_per_split = 1;
+    r.n_splits = 0;
+    return r;
+  }
+  r.tile0 = r.lo / ts;
+  r.n_tiles = (r.hi + ts - 1) / ts - r.tile0;
+  r.tiles_per_split = p.fixed_splits > 0 ? (r.n_tiles + p.fixed_splits - 1) / p.fixed_splits : p.split_tiles;
+  r.n_splits = (r.n_tiles + r.tiles_per_split - 1) / r.tiles_per_split;
+  return r;
+}
+
+template <int D, bool FP8, int NH8, int TS, int NS>
+struct Traits {
+  static constexpr int E = FP8 ? 1 : 2;                        // bytes per element
+  static constexpr int ROW = D * E;                            // bytes of one key row of one head
+  static constexpr int RB = ROW < 128 ? ROW : 128;             // bytes per TMA box row
+  static constexpr int NCC = ROW / RB;                         // column chunks per row
+  static constexpr int TILE = TS * ROW;                        // K (or V) bytes per stage
+  static constexpr int STAGE = 2 * TILE;
+  static constexpr int WARP_BYTES = NS * STAGE;
+  static constexpr int MT = TS / 16;                           // 16-key groups per tile
+  static constexpr int KS = D / 16;                            // 16-wide steps over head_dim
+  static constexpr int HW = NH8 * 8;                           // heads per warp (MMA N)
+  static_assert(RB == 128 || RB == 64, "row bytes must use the 128B or 64B swizzle");
+  static_assert(TS % 16 == 0, "tile must hold whole 16-key groups");
+
+  // Byte offset of (row, byte-in-row) inside a K or V stage tile as TMA
+  // writes it: column chunks of RB bytes, rows of RB bytes, 16-byte units
+  // XOR-swizzled (128B swizzle: unit ^= row & 7; 64B swizzle: unit ^= (row>>1) & 3).
+  __device__ static __forceinline__ uint32_t off(int row, int byte) {
+    const int cc = byte / RB;
+    const int x = byte % RB;
+    const uint32_t sw = (RB == 128) ? (row & 7) : ((row >> 1) & 3);
+    return static_cast<uint32_t>(cc * (TS * RB) + row * RB) + ((((x >> 4) ^ sw) << 4) | (x & 15));
+  }
+};
+
+template <int D, bool FP8, int NH8, int TS, int NS>
+__global__ void __launch_bounds__(kWarps * 32)
+decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                    const DecodeParams p) {
+  using T = Traits<D, FP8, NH8, TS, NS>;
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y;
+  const int b = blockIdx.z;
+  const int L = p.seq_lens[b];
+  const SplitRange r = split_range(p, L);
+  if (split >= r.n_splits) return;
+  if (r.n_splits > p.max_splits) {  // seq_lens beyond the planned capacity
+    if (threadIdx.x == 0 && split == 0) atomicOr(p.err, kErrCapacity);
+    return;
+  }
+
+  const int tile_begin = r.tile0 + split * r.tiles_per_split;
+  const int tile_end = min(tile_begin + r.tiles_per_split, r.tile0 + r.n_tiles);
+  const int n_tiles = tile_end - tile_begin;
+  const int tok_lo = max(r.lo, tile_begin * TS);
+  const int tok_hi = min(r.hi, tile_end * TS);
+  const int ps = p.page_size;
+  const int pg0 = (tile_begin * TS) / ps;
+  const int pg1 = (tok_hi + ps - 1) / ps;   // <= ceil(L / ps): never past the request's pages
+  const int G = p.group;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * T::WARP_BYTES);
+  int32_t* bt_s = reinterpret_cast<int32_t*>(bars + kWarps * NS);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int g = lane >> 2;   // MMA group id
+  const int c = lane & 3;    // thread in group
+
+  if (pg1 - pg0 > p.bt_cache) {  // planner invariant; never expected
+    if (tid == 0) atomicOr(p.err, kErrSchedOverflow);
+    return;
+  }
+  const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+  for (int i = tid; i < pg1 - pg0; i += kWarps * 32) bt_s[i] = bt_row[pg0 + i];
+  if (tid == 0) {
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+    for (int i = 0; i < kWarps * NS; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  uint8_t* wbase = smem + warp * T::WARP_BYTES;
+  uint64_t* wbar = bars + warp * NS;
+
+  // Lane 0: fetch local tile k of this split into `stage` (K and V, all
+  // pages the tile touches, every column chunk).  Boxes wholly past the end
+  // of the sequence are not fetched; their rows are masked.
+  auto issue = [&](int k, int stage) {
+    const int t0 = (tile_begin + k) * TS;
+    const int br = ps < TS ? ps : TS;
+    int nb = 0;
+    for (int j = 0; j < TS / br; ++j) nb += (t0 + j * br < L) ? 1 : 0;
+    uint8_t* kst = wbase + stage * T::STAGE;
+    uint8_t* vst = kst + T::TILE;
+    mbar_arrive_expect_tx(&wbar[stage], static_cast<uint32_t>(nb * br * T::ROW * 2));
+    for (int j = 0; j < nb; ++j) {
+      const int t = t0 + j * br;
+      const int page = bt_s[t / ps - pg0];
+      const int slot = t % ps;
+#pragma unroll
+      for (int cc = 0; cc < T::NCC; ++cc) {
+        const int dst = cc * TS * T::RB + j * br * T::RB;
+        tma_load_4d(kst + dst, &tmk, cc * (T::RB / T::E), kvh, slot, page, &wbar[stage]);
+        tma_load_4d(vst + dst, &tmv, cc * (T::RB / T::E), kvh, slot, page, &wbar[stage]);
+      }
+    }
+  };
+
+  // Q^T fragments (MMA B operand: k = head_dim slot, n = head).
+  uint32_t qf[T::KS][NH8][2];
+  {
+    const uint16_t* qb = p.q + static_cast<int64_t>(b) * p.q_stride_tok;
+#pragma unroll
+    for (int j = 0; j < NH8; ++j) {
+      const int hh = j * 8 + g;
+      const bool ok = hh < G;
+      const uint16_t* qh = qb + static_cast<int64_t>(kvh * G + (ok ? hh : 0)) * p.q_stride_head;
+#pragma unroll
+      for (int ks = 0; ks < T::KS; ++ks) {
+        int d0, d1;
+        if constexpr (FP8) {   // permuted head_dim: thread c owns dims [c*D/4, (c+1)*D/4)
+          d0 = c * (D / 4) + ks * 4;
+          d1 = d0 + 2;
+        } else {
+          d0 = ks * 16 + 2 * c;
+          d1 = d0 + 8;
+        }
+        qf[ks][j][0] = ok ? *reinterpret_cast<const uint32_t*>(qh + d0) : 0u;
+        qf[ks][j][1] = ok ? *reinterpret_cast<const uint32_t*>(qh + d1) : 0u;
+      }
+    }
+  }
+
+  float o[T::KS][NH8][4];
+#pragma unroll
+  for (int i = 0; i < T::KS; ++i)
+#pragma unroll
+    for (int j = 0; j < NH8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[i][j][e] = 0.f;
+  float m_run[NH8][2], l_run[NH8][2];
+#pragma unroll
+  for (int j = 0; j < NH8; ++j) {
+    m_run[j][0] = m_run[j][1] = -INFINITY;
+    l_run[j][0] = l_run[j][1] = 0.f;
+  }
+
+  if (lane == 0) {
+    for (int s = 0; s < NS; ++s) {
+      const int k = warp + s * kWarps;
+      if (k < n_tiles) issue(k, s);
+    }
+  }
+  __syncwarp();
+
+  const bool capped = p.cap_log2 > 0.f;
+  int it = 0;
+  for (int k = warp; k < n_tiles; k += kWarps, ++it) {
+    const int stage = it % NS;
+    const uint32_t parity = static_cast<uint32_t>((it / NS) & 1);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&wbar[stage], parity, p.err));
+    if (!ok) break;
+    const uint8_t* kst = wbase + stage * T::STAGE;
+    const uint8_t* vst = kst + T::TILE;
+    const uint32_t kst_u = smem_u32(kst);
+    const uint32_t vst_u = smem_u32(vst);
+    const int t0 = (tile_begin + k) * TS;
+    const bool partial = (t0 < tok_lo) || (t0 + TS > tok_hi);
+
+    // ---- S^T = K Q^T ------------------------------------------------------
+    float s[T::MT][NH8][4];
+#pragma unroll
+    for (int mt = 0; mt < T::MT; ++mt) {
+#pragma unroll
+      for (int j = 0; j < NH8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[mt][j][e] = 0.f;
+      if constexpr (!FP8) {
+        const int mi = lane >> 3, rr = lane & 7;
+        const int tok = mt * 16 + rr + ((mi & 1) << 3);
+#pragma unroll
+        for (int ks = 0; ks < T::KS; ++ks) {
+          uint32_t a[4];
+          ldsm_x4(a, kst_u + T::off(tok, (ks * 16 + ((mi >> 1) << 3)) * 2));
+#pragma unroll
+          for (int j = 0; j < NH8; ++j) mma_bf16(s[mt][j], a, qf[ks][j][0], qf[ks][j][1]);
+        }
+      } else {
+        constexpr int NV = D / 64;  // 16-byte units per thread per row
+        uint4 r0[NV], r1[NV];
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+          r0[u] = *reinterpret_cast<const uint4*>(kst + T::off(mt * 16 + g, c * (D / 4) + 16 * u));
+          r1[u] = *reinterpret_cast<const uint4*>(kst + T::off(mt * 16 + g + 8, c * (D / 4) + 16 * u));
+        }
+        const uint32_t* w0 = reinterpret_cast<const uint32_t*>(r0);
+        const uint32_t* w1 = reinterpret_cast<const uint32_t*>(r1);
+#pragma unroll
+        for (int ks = 0; ks < T::KS; ++ks) {
+          uint32_t a[4];
+          a[0] = dequant_e4m3x2(w0[ks], p.k_scale);
+          a[1] = dequant_e4m3x2(w1[ks], p.k_scale);
+          a[2] = dequant_e4m3x2(w0[ks] >> 16, p.k_scale);
+          a[3] = dequant_e4m3x2(w1[ks] >> 16, p.k_scale);
+#pragma unroll
+          for (int j = 0; j < NH8; ++j) mma_bf16(s[mt][j], a, qf[ks][j][0], qf[ks][j][1]);
+        }
+      }
+    }
+
+    // ---- scale, soft-cap, mask; online softmax (log2 domain) ----------------
+    float mx[NH8][2];
+#pragma unroll
+    for (int j = 0; j < NH8; ++j) mx[j][0] = mx[j][1] = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < T::MT; ++mt)
+#pragma unroll
+      for (int j = 0; j < NH8; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float v = s[mt][j][e];
+          v = capped ? p.cap_log2 * tanhf(v * p.scale_over_cap) : v * p.scale_log2;
+          if (partial) {
+            const int tok = t0 + mt * 16 + g + ((e >> 1) << 3);
+            if (tok < tok_lo || tok >= tok_hi) v = -INFINITY;
+          }
+          s[mt][j][e] = v;
+          mx[j][e & 1] = fmaxf(mx[j][e & 1], v);
+        }
+    float alpha[NH8][2], mu[NH8][2];
+#pragma unroll
+    for (int j = 0; j < NH8; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float m = mx[j][h];
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        const float m_new = fmaxf(m_run[j][h], m);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        alpha[j][h] = ex2(m_run[j][h] - m_use);
+        m_run[j][h] = m_new;
+        mu[j][h] = m_use;
+      }
+#pragma unroll
+    for (int j = 0; j < NH8; ++j) {
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < T::MT; ++mt) {
+        s[mt][j][0] = ex2(s[mt][j][0] - mu[j][0]);
+        s[mt][j][1] = ex2(s[mt][j][1] - mu[j][1]);
+        s[mt][j][2] = ex2(s[mt][j][2] - mu[j][0]);
+        s[mt][j][3] = ex2(s[mt][j][3] - mu[j][1]);
+        ls0 += s[mt][j][0] + s[mt][j][2];
+        ls1 += s[mt][j][1] + s[mt][j][3];
+      }
+      l_run[j][0] = l_run[j][0] * alpha[j][0] + ls0;
+      l_run[j][1] = l_run[j][1] * alpha[j][1] + ls1;
+#pragma unroll
+      for (int i = 0; i < T::KS; ++i) {
+        o[i][j][0] *= alpha[j][0];
+        o[i][j][1] *= alpha[j][1];
+        o[i][j][2] *= alpha[j][0];
+        o[i][j][3] *= alpha[j][1];
+      }
+    }
+
+    // ---- O^T += V^T P^T -----------------------------------------------------
+#pragma unroll
+    for (int mt = 0; mt < T::MT; ++mt) {
+      uint32_t pb[NH8][2];
+#pragma unroll
+      for (int j = 0; j < NH8; ++j) {
+        pb[j][0] = movmatrix_t(pack_bf16x2(s[mt][j][0], s[mt][j][1]));
+        pb[j][1] = movmatrix_t(pack_bf16x2(s[mt][j][2], s[mt][j][3]));
+      }
+      // Masked keys have P = 0, but their V rows may be stale or NaN: zero
+      // them in the fragment so 0 * NaN never reaches the accumulator.
+      uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+      if (partial) {
+        const int tk = t0 + mt * 16 + 2 * c;
+        auto valid = [&](int t) { return t >= tok_lo && t < tok_hi; };
+        vm_lo = (valid(tk) ? 0x0000ffffu : 0u) | (valid(tk + 1) ? 0xffff0000u : 0u);
+        vm_hi = (valid(tk + 8) ? 0x0000ffffu : 0u) | (valid(tk + 9) ? 0xffff0000u : 0u);
+      }
+      if constexpr (!FP8) {
+        const int mi = lane >> 3, rr = lane & 7;
+        const int tok = mt * 16 + rr + ((mi >> 1) << 3);
+#pragma unroll
+        for (int i = 0; i < T::KS; ++i) {
+          uint32_t a[4];
+          ldsm_x4_t(a, vst_u + T::off(tok, (i * 16 + ((mi & 1) << 3)) * 2));
+          a[0] &= vm_lo;
+          a[1] &= vm_lo;
+          a[2] &= vm_hi;
+          a[3] &= vm_hi;
+#pragma unroll
+          for (int j = 0; j < NH8; ++j) mma_bf16(o[i][j], a, pb[j][0], pb[j][1]);
+        }
+      } else {
+        // thread g owns output dims [g*D/8, (g+1)*D/8): m-tile i row g -> dim
+        // g*D/8 + 2i, row g+8 -> g*D/8 + 2i + 1.
+        constexpr int NW = D / 32;  // 32-bit words per thread per row
+        uint32_t ra[NW], rb[NW], rc[NW], rd[NW];
+        const int rowa = mt * 16 + 2 * c;
+#pragma unroll
+        for (int u = 0; u < NW; u += 2) {
+          const int byte = g * (D / 8) + 4 * u;
+          const uint2 xa = *reinterpret_cast<const uint2*>(vst + T::off(rowa, byte));
+          const uint2 xb = *reinterpret_cast<const uint2*>(vst + T::off(rowa + 1, byte));
+          const uint2 xc = *reinterpret_cast<const uint2*>(vst + T::off(rowa + 8, byte));
+          const uint2 xd = *reinterpret_cast<const uint2*>(vst + T::off(rowa + 9, byte));
+          ra[u] = xa.x; ra[u + 1] = xa.y;
+          rb[u] = xb.x; rb[u + 1] = xb.y;
+          rc[u] = xc.x; rc[u + 1] = xc.y;
+          rd[u] = xd.x; rd[u + 1] = xd.y;
+        }
+#pragma unroll
+        for (int i = 0; i < T::KS; ++i) {
+          const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+          const uint32_t x = __byte_perm(ra[i >> 1], rb[i >> 1], sel);
+          const uint32_t y = __byte_perm(rc[i >> 1], rd[i >> 1], sel);
+          uint32_t a[4];
+          a[0] = dequant_e4m3x2(x, p.v_scale) & vm_lo;
+          a[1] = dequant_e4m3x2(x >> 16, p.v_scale) & vm_lo;
+          a[2] = dequant_e4m3x2(y, p.v_scale) & vm_hi;
+          a[3] = dequant_e4m3x2(y >> 16, p.v_scale) & vm_hi;
+#pragma unroll
+          for (int j = 0; j < NH8; ++j) mma_bf16(o[i][j], a, pb[j][0], pb[j][1]);
+        }
+      }
+    }
+
+    __syncwarp();
+    const int kn = k + NS * kWarps;
+    if (lane == 0 && kn < n_tiles) {
+      fence_proxy_async_smem();
+      issue(kn, stage);
+    }
+  }
+
+  // ---- merge the 4 warps' states in shared memory ----------------------------
+  // Every TMA a warp issued was waited for inside its loop, so its stage
+  // buffers are free; each warp writes its state into its own region.
+  float* wo = reinterpret_cast<float*>(wbase);   // [HW][D]
+  float* wm = wo + T::HW * D;                     // [HW]
+  float* wl = wm + T::HW;                         // [HW]
+#pragma unroll
+  for (int j = 0; j < NH8; ++j)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float l = l_run[j][h];
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      if (g == 0) {
+        wm[j * 8 + 2 * c + h] = m_run[j][h];
+        wl[j * 8 + 2 * c + h] = l;
+      }
+    }
+#pragma unroll
+  for (int i = 0; i < T::KS; ++i)
+#pragma unroll
+    for (int j = 0; j < NH8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int h = j * 8 + 2 * c + (e & 1);
+        const int d = FP8 ? (g * (D / 8) + 2 * i + (e >> 1)) : (16 * i + g + ((e >> 1) << 3));
+        wo[h * D + d] = o[i][j][e];
+      }
+  __syncthreads();
+
+  const bool direct = (r.n_splits == 1);
+  for (int e = tid; e < G * D; e += kWarps * 32) {
+    const int h = e / D;
+    const int d = e - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float* ww = reinterpret_cast<const float*>(smem + w * T::WARP_BYTES) + T::HW * D;
+      M = fmaxf(M, ww[h]);
+    }
+    if (M == -INFINITY) M = 0.f;
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float* wob = reinterpret_cast<const float*>(smem + w * T::WARP_BYTES);
+      const float f = ex2(wob[T::HW * D + h] - M);
+      num += wob[h * D + d] * f;
+      den += wob[T::HW * D + T::HW + h] * f;
+    }
+    const int hq = kvh * G + h;
+    if (direct) {
+      float M2 = M, zs = 0.f;
+      if (p.sinks != nullptr) {
+        const float sk = p.sinks[hq] * kLog2e;
+        M2 = fmaxf(M, sk);
+        zs = ex2(sk - M2);
+      }
+      const float f = ex2(M - M2);
+      const float Z = den * f + zs;
+      const float ov = (Z > 0.f) ? num * f / Z : 0.f;
+      p.out[static_cast<int64_t>(b) * p.out_stride_tok + static_cast<int64_t>(hq) * p.out_stride_head + d] =
+          __bfloat16_as_ushort(__float2bfloat16_rn(ov));
+      if (d == 0 && p.lse != nullptr) p.lse[static_cast<int64_t>(b) * p.num_q_heads + hq] = (M2 + lg2(Z)) * kLn2;
+    } else {
+      const int64_t row = (static_cast<int64_t>(b) * p.num_q_heads + hq) * p.max_splits + split;
+      p.o_part[row * D + d] = (den > 0.f) ? num / den : 0.f;
+      if (d == 0) p.lse_part[row] = (M + lg2(den)) * kLn2;
+    }
+  }
+}
+
+// LSE merge: one warp per (request, q head); lane owns D/32 consecutive dims.
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p) {
+  const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (wid >= p.batch * p.num_q_heads) return;
+  const int b = wid / p.num_q_heads;
+  const int hq = wid - b * p.num_q_heads;
+  const SplitRange r = split_range(p, p.seq_lens[b]);
+  if (r.n_splits == 1) return;  // written by the split kernel
+  if (r.n_splits > p.max_splits) {  // seq_lens beyond the planned capacity
+    if (lane == 0) atomicOr(p.err, kErrCapacity);
+    return;
+  }
+  constexpr int V = D / 32;
+  const bool has_sink = p.sinks != nullptr;
+  const float sk = has_sink ? p.sinks[hq] * kLog2e : -INFINITY;
+  uint16_t* outp = p.out + static_cast<int64_t>(b) * p.out_stride_tok + static_cast<int64_t>(hq) * p.out_stride_head;
+  float acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = 0.f;
+  float M = sk;
+  const int64_t row0 = (static_cast<int64_t>(b) * p.num_q_heads + hq) * p.max_splits;
+  for (int s = lane; s < r.n_splits; s += 32) M = fmaxf(M, p.lse_part[row0 + s] * kLog2e);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float Z = 0.f;
+  if (M != -INFINITY) {
+    Z = has_sink ? ex2(sk - M) : 0.f;
+    for (int s = 0; s < r.n_splits; ++s) {
+      const float w = ex2(p.lse_part[row0 + s] * kLog2e - M);
+      Z += w;
+      const float* op = p.o_part + (row0 + s) * D + lane * V;
+#pragma unroll
+      for (int v = 0; v < V; v += 2) {
+        const float2 x = *reinterpret_cast<const float2*>(op + v);
+        acc[v] += w * x.x;
+        acc[v + 1] += w * x.y;
+      }
+    }
+  }
+  const float inv = (Z > 0.f) ? 1.f / Z : 0.f;
+#pragma unroll
+  for (int v = 0; v < V; v += 2) {
+    *reinterpret_cast<uint32_t*>(outp + lane * V + v) = pack_bf16x2(acc[v] * inv, acc[v + 1] * inv);
+  }
+  if (lane == 0 && p.lse != nullptr) {
+    p.lse[static_cast<int64_t>(b) * p.num_q_heads + hq] = (M == -INFINITY) ? -INFINITY : (M + lg2(Z)) * kLn2;
+  }
+}
+
+template <int D, bool FP8, int NH8, int TS, int NS>
+cudaError_t launch_variant(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p, dim3 grid,
+                           int smem, cudaStream_t stream) {
+  auto kern = decode_split_kernel<D, FP8, NH8, TS, NS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  if (grid.x > 0 && grid.y > 0 && grid.z > 0) {
+    kern<<<grid, kWarps * 32, smem, stream>>>(tmk, tmv, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int warps = p.batch * p.num_q_heads;
+  if (warps > 0) {
+    decode_merge_kernel<D><<<(warps + 3) / 4, 128, 0, stream>>>(p);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+template <int D, bool FP8>
+struct TileChoice;
+// Keys per stage and stages per warp: about 8-16 KB per stage, 3-4 stages.
+template <> struct TileChoice<64, false> { static constexpr int TS = 16, NS = 4; };
+template <> struct TileChoice<128, false> { static constexpr int TS = 16, NS = 3; };
+template <> struct TileChoice<256, false> { static constexpr int TS = 16, NS = 3; };
+template <> struct TileChoice<64, true> { static constexpr int TS = 64, NS = 3; };
+template <> struct TileChoice<128, true> { static constexpr int TS = 32, NS = 3; };
+template <> struct TileChoice<256, true> { static constexpr int TS = 16, NS = 3; };
+
+template <int D, bool FP8>
+int smem_for(int bt_cache) {
+  using C = TileChoice<D, FP8>;
+  using T = Traits<D, FP8, 1, C::TS, C::NS>;
+  return 1024 + kWarps * T::WARP_BYTES + kWarps * C::NS * 8 + bt_cache * 4;
+}
+
+template <int D, bool FP8>
+cudaError_t launch_d(const DecodeConfig& cfg, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                     const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+  using C = TileChoice<D, FP8>;
+  if (cfg.nh8 == 1) return launch_variant<D, FP8, 1, C::TS, C::NS>(tmk, tmv, p, grid, cfg.smem_bytes, stream);
+  return launch_variant<D, FP8, 2, C::TS, C::NS>(tmk, tmv, p, grid, cfg.smem_bytes, stream);
+}
+
+}  // namespace
+
+DecodeConfig decode_config(int head_dim, bool fp8, int group, int bt_cache) {
+  DecodeConfig c{};
+  c.head_dim = head_dim;
+  c.fp8 = fp8;
+  c.nh8 = group <= 8 ? 1 : 2;
+  c.warps = kWarps;
+#define PA_TILE_CASE(DD, F8)                                    \
+  if (head_dim == DD && fp8 == F8) {                            \
+    c.tile_tokens = TileChoice<DD, F8>::TS;                     \
+    c.stages = TileChoice<DD, F8>::NS;                          \
+    c.smem_bytes = smem_for<DD, F8>(bt_cache);                  \
+  }
+  PA_TILE_CASE(64, false)
+  PA_TILE_CASE(128, false)
+  PA_TILE_CASE(256, false)
+  PA_TILE_CASE(64, true)
+  PA_TILE_CASE(128, true)
+  PA_TILE_CASE(256, true)
+#undef PA_TILE_CASE
+  return c;
+}
+
+cudaError_t launch_decode(const DecodeConfig& cfg, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                          const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+  switch (cfg.head_dim) {
+    case 64: return cfg.fp8 ? launch_d<64, true>(cfg, tmk, tmv, p, grid, stream)
+                            : launch_d<64, false>(cfg, tmk, tmv, p, grid, stream);
+    case 128: return cfg.fp8 ? launch_d<128, true>(cfg, tmk, tmv, p, grid, stream)
+                             : launch_d<128, false>(cfg, tmk, tmv, p, grid, stream);
+    case 256: return cfg.fp8 ? launch_d<256, true>(cfg, tmk, tmv, p, grid, stream)
+                             : launch_d<256, false>(cfg, tmk, tmv, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pa

@@ -1,0 +1,62 @@
+// Internal declarations shared by the CUDA translation units of the library.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+// Scratch header: the first 256 bytes of every scratch workspace.
+constexpr int64_t kScratchHeaderBytes = 256;
+// Device error codes OR-ed into the header's first word.
+constexpr uint32_t kErrWaitTimeout = 1u;        // an mbarrier wait ran out of time
+constexpr uint32_t kErrSchedOverflow = 2u;      // extend work list exceeded its capacity
+constexpr uint32_t kErrCapacity = 4u;           // a length exceeded the plan's capacity
+// Wall-clock bound on every device-side wait (nanoseconds of %globaltimer).
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+// Decode launch parameters (by value to both decode kernels).
+struct DecodeParams {
+  const uint16_t* q;          // bf16 [B, Hq, D]
+  int64_t q_stride_tok, q_stride_head;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* seq_lens;
+  int batch, num_q_heads, num_kv_heads, group, page_size;
+  float scale_log2;           // scale * log2(e)
+  float cap_log2;             // soft_cap * log2(e); 0 = off
+  float scale_over_cap;       // scale / soft_cap
+  int window;                 // 0 = off
+  const float* sinks;         // [Hq] or null
+  float k_scale, v_scale;
+  uint16_t* out;              // bf16 [B, Hq, D]
+  int64_t out_stride_tok, out_stride_head;
+  float* lse;                 // [B, Hq] or null
+  float* o_part;              // [B, Hq, max_splits, D] normalised split outputs
+  float* lse_part;            // [B, Hq, max_splits] split LSE (natural log)
+  int tile_tokens;            // keys per pipeline stage
+  int max_splits;
+  int split_tiles;            // >0: tiles per split (planner mode)
+  int fixed_splits;           // >0: split count per request (fixed mode)
+  int bt_cache;               // block-table entries staged per CTA
+  uint32_t* err;              // scratch header error word
+};
+
+struct DecodeConfig {
+  int head_dim;
+  bool fp8;
+  int nh8;                    // ceil(group / 8)
+  int tile_tokens;
+  int stages;
+  int warps;
+  int smem_bytes;
+};
+
+// Kernel-variant table shared by the planner and the launcher.
+DecodeConfig decode_config(int head_dim, bool fp8, int group, int bt_cache);
+
+cudaError_t launch_decode(const DecodeConfig& cfg, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                          const DecodeParams& p, dim3 grid, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,185 @@
+"""The C-ABI library: it builds, loads, exports every symbol include/*.h
+declares, and its host-side logic (planning, argument checks) behaves, all
+without a GPU."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from paged_kv_gqa_12_gb300 import binding as pb
+from paged_kv_gqa_12_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return pb.load()
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s*(pa_\w+)\s*\(", src, flags=re.M))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"pa_plan", "pa_decode", "pa_extend", "pa_check", "pa_scratch_init"} <= names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(pb.EXPORTED_SYMBOLS) <= names
+
+
+def test_version_and_strings(lib):
+    assert lib.pa_version() >= 100
+    for s in range(6):
+        assert pb.status_string(s)
+
+
+def _plan(**kw):
+    base = dict(mode=pb.MODE_DECODE, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                max_batch=64, max_pages_per_seq=512, num_sms=152)
+    base.update(kw)
+    return pb.plan(**base)
+
+
+def test_plan_decode_defaults(lib):
+    p = _plan()
+    assert p.tile_tokens in (16, 32, 64)
+    assert p.max_splits >= 1 and p.split_tiles >= 1
+    assert p.grid[0] == p.max_splits and p.grid[1] == 8 and p.grid[2] == 64
+    assert p.scratch_bytes >= 256 + 64 * 32 * p.max_splits * (128 + 1) * 4
+    assert p.smem_bytes <= 232448
+
+
+def test_plan_uses_host_lengths(lib):
+    short = _plan(host_seq_lens=[600] * 64)
+    long = _plan(host_seq_lens=[8000] * 64)
+    assert long.split_tiles >= short.split_tiles
+
+
+def test_plan_fixed_splits(lib):
+    p = _plan(num_splits=4, max_pages_per_seq=19)
+    assert p.max_splits == 4 and p.split_tiles == 0
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(num_q_heads=30), pb.PA_ERR_INVALID_ARG),         # Hq % Hkv != 0
+    (dict(head_dim=96), pb.PA_ERR_UNSUPPORTED),
+    (dict(page_size=8), pb.PA_ERR_UNSUPPORTED),
+    (dict(num_q_heads=136, num_kv_heads=8), pb.PA_ERR_UNSUPPORTED),  # group 17
+    (dict(window=-1), pb.PA_ERR_INVALID_ARG),
+    (dict(soft_cap=-1.0), pb.PA_ERR_INVALID_ARG),
+    (dict(soft_cap=float("inf")), pb.PA_ERR_INVALID_ARG),
+    (dict(kv_dtype=7), pb.PA_ERR_INVALID_ARG),
+    (dict(mode=5), pb.PA_ERR_INVALID_ARG),
+    (dict(host_seq_lens=[10, -1]), pb.PA_ERR_INVALID_ARG),
+    (dict(host_seq_lens=[512 * 16 + 1]), pb.PA_ERR_INVALID_ARG),
+])
+def test_plan_rejects(lib, bad, status):
+    with pytest.raises(pb.PaError) as ei:
+        _plan(**bad)
+    assert ei.value.status == status
+
+
+class _Fake:
+    """A stand-in tensor with a fixed fake address: only host-side checks
+    that fail before any CUDA call are exercised with it."""
+
+    def __init__(self, addr, shape=(4, 8, 128), strides=None, itemsize=2):
+        self._addr = addr
+        self.shape = shape
+        self._strides = strides or tuple(int(x) for x in _contig(shape))
+        self._itemsize = itemsize
+
+    def data_ptr(self):
+        return self._addr
+
+    def stride(self, i=None):
+        return self._strides if i is None else self._strides[i]
+
+    def dim(self):
+        return len(self.shape)
+
+    def numel(self):
+        n = 1
+        for s in self.shape:
+            n *= s
+        return n
+
+    def element_size(self):
+        return self._itemsize
+
+
+def _contig(shape):
+    st, acc = [], 1
+    for s in reversed(shape):
+        st.append(acc)
+        acc *= s
+    return list(reversed(st))
+
+
+def _decode_args(plan, **over):
+    a = dict(plan=plan, q=0x10000, qs=(32 * 128, 128), k=0x20000, v=0x40000, kvs=(16 * 8 * 128, 8 * 128, 128),
+             pages=100, bt=0x50000, bts=512, sl=0x60000, batch=4, scale=0.088, sinks=None, ks=1.0, vs=1.0,
+             out=0x70000, os=(32 * 128, 128), lse=None, scratch=0x100000, sbytes=plan.scratch_bytes, stream=None)
+    a.update(over)
+    L = pb.load()
+    vp = ctypes.c_void_p
+    return L.pa_decode(ctypes.byref(a["plan"]), vp(a["q"]), a["qs"][0], a["qs"][1], vp(a["k"]), vp(a["v"]),
+                       a["kvs"][0], a["kvs"][1], a["kvs"][2], a["pages"], vp(a["bt"]), a["bts"], vp(a["sl"]),
+                       a["batch"], a["scale"], vp(a["sinks"]) if a["sinks"] else None, a["ks"], a["vs"],
+                       vp(a["out"]), a["os"][0], a["os"][1], vp(a["lse"]) if a["lse"] else None,
+                       vp(a["scratch"]) if a["scratch"] else None, a["sbytes"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(batch=65), pb.PA_ERR_INVALID_ARG),
+    (dict(batch=-1), pb.PA_ERR_INVALID_ARG),
+    (dict(sbytes=255), pb.PA_ERR_SCRATCH_TOO_SMALL),
+    (dict(scratch=0), pb.PA_ERR_INVALID_ARG),
+    (dict(scratch=0x100010), pb.PA_ERR_UNSUPPORTED),        # scratch not 256-byte aligned
+    (dict(sinks=0x80000), pb.PA_ERR_INVALID_ARG),           # plan has no sinks
+    (dict(scale=float("nan")), pb.PA_ERR_INVALID_ARG),
+    (dict(q=0), pb.PA_ERR_INVALID_ARG),
+    (dict(q=0x10002), pb.PA_ERR_UNSUPPORTED),               # q not 4-byte aligned
+    (dict(k=0x20008), pb.PA_ERR_UNSUPPORTED),               # cache not 16-byte aligned
+    (dict(kvs=(16 * 8 * 128, 8 * 128 + 4, 128)), pb.PA_ERR_UNSUPPORTED),  # token stride not 16B multiple
+    (dict(pages=0), pb.PA_ERR_INVALID_ARG),
+    (dict(bt=0), pb.PA_ERR_INVALID_ARG),
+    (dict(out=0), pb.PA_ERR_INVALID_ARG),
+])
+def test_decode_rejects_before_launch(lib, over, status):
+    plan = _plan()
+    assert _decode_args(plan, **over) == status
+
+
+def test_decode_empty_batch_is_noop(lib):
+    plan = _plan()
+    assert _decode_args(plan, batch=0) == pb.PA_OK
+
+
+def test_decode_rejects_extend_plan(lib):
+    try:
+        plan = _plan(mode=pb.MODE_EXTEND, max_total_q=1024)
+    except pb.PaError:
+        pytest.skip("extend planning unavailable")
+    assert _decode_args(plan) == pb.PA_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import importlib
+    b2 = importlib.reload(pb)
+    try:
+        b2._lib = None
+        with pytest.raises(RuntimeError):
+            b2.load(str(tmp_path / "missing.so"))
+    finally:
+        importlib.reload(pb)

@@ -1,0 +1,159 @@
+"""Decode parity: the CUDA split-KV path (through the C ABI) against the oracle."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_gqa_12_gb300 import workloads as wl
+from tests import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_gqa_12_gb300 import binding
+    binding.load()
+
+
+def _small(seed, *, Hq, Hkv, D, ps, lens, kv="bf16", **kw):
+    extra = {}
+    if kv == "fp8_e4m3":
+        extra = dict(k_scale=0.05, v_scale=0.05)
+    return wl.build_problem("decode", num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=ps,
+                            seq_lens=lens, kv_dtype=kv, seed=seed, **extra, **kw)
+
+
+LENS = [1, 15, 16, 17, 63, 200, 777, 1500]
+
+VARIANTS = [
+    # Hq, Hkv, D, ps, kv
+    (8, 2, 64, 16, "bf16"),
+    (32, 8, 128, 16, "bf16"),
+    (16, 8, 256, 32, "bf16"),
+    (64, 8, 64, 64, "fp8_e4m3"),
+    (16, 4, 128, 32, "fp8_e4m3"),
+    (4, 2, 256, 16, "fp8_e4m3"),
+    (16, 1, 128, 16, "bf16"),       # group 16: two 8-head MMA columns
+    (12, 1, 64, 32, "bf16"),        # group 12: padded heads
+    (4, 4, 128, 64, "bf16"),        # group 1 (MHA)
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,ps,kv", VARIANTS)
+@pytest.mark.parametrize("opts", [{}, {"window": 70, "sinks": True}, {"soft_cap": 5.0, "window": 300}])
+def test_decode_variants(Hq, Hkv, D, ps, kv, opts):
+    p = _small(Hq * 7 + D + ps, Hq=Hq, Hkv=Hkv, D=D, ps=ps, lens=LENS, kv=kv, **opts)
+    ref_o, ref_l = oracle.attention(p)
+    for ns in (0, 1, 3):
+        out, lse = gh.run(p, num_splits=ns)
+        gh.assert_parity(out, lse, ref_o, ref_l, what=f"splits={ns}")
+
+
+def test_config1_split_counts():
+    p = wl.config_problem(1)
+    ref_o, ref_l = oracle.attention(p)
+    for ns in (4, 1, 2, 3, 7, 0):
+        out, lse = gh.run(p, num_splits=ns)
+        gh.assert_parity(out, lse, ref_o, ref_l, what=f"config1 splits={ns}")
+
+
+def test_split_invariance_close():
+    # Different split counts give the same answer up to fp32 re-association.
+    p = _small(5, Hq=32, Hkv=8, D=128, ps=16, lens=[5000, 3000, 129])
+    outs = [gh.run(p, num_splits=ns) for ns in (1, 2, 5, 16, 0)]
+    for o, l in outs[1:]:
+        assert np.abs(o - outs[0][0]).max() <= 1e-2
+        assert np.abs(l - outs[0][1]).max() <= 1e-4
+
+
+def test_identity_probe_window_one_bitwise():
+    # window = 1: each query sees only its own key -> out == V row exactly,
+    # with NaN in every unattended slot of the pool.
+    for (Hq, Hkv, D, ps, kv) in VARIANTS:
+        p = _small(11 + D, Hq=Hq, Hkv=Hkv, D=D, ps=ps, lens=LENS, kv=kv, window=1, keep_logical=True)
+        out, _ = gh.run(p)
+        ref_o, _ = oracle.attention(p)
+        assert np.array_equal(out.astype(np.float64), ref_o), (Hq, Hkv, D, ps, kv)
+
+
+def test_onehot_query_reads_exact_key():
+    # q = e_d (head h probes dim d = (7h) mod D), scale 1, window 1: the LSE is
+    # the dequantised K element at the query's own position.  The kernel's
+    # softmax runs in the log2 domain, so LSE = (s*log2 e)*ln 2 may differ from
+    # s by a few fp32 ulps; any wrong element differs by >= a bf16 ulp (2^-8).
+    for kv in ("bf16", "fp8_e4m3"):
+        Hq, Hkv, D, ps = 16, 2, 128, 16
+        T = len(LENS)
+        qv = np.zeros((T, Hq, D), np.float32)
+        dims = [(7 * h) % D for h in range(Hq)]
+        for h in range(Hq):
+            qv[:, h, dims[h]] = 1.0
+        p = _small(21, Hq=Hq, Hkv=Hkv, D=D, ps=ps, lens=LENS, kv=kv, window=1, q_values=qv)
+        p.scale = 1.0
+        _, lse = gh.run(p)
+        _, ref_l = oracle.attention(p)
+        err = np.abs(lse.astype(np.float64) - ref_l)
+        assert np.all(err <= 4 * np.spacing(np.abs(ref_l).astype(np.float32))), (kv, err.max())
+
+
+def test_page_permutation_bitwise():
+    p = _small(31, Hq=32, Hkv=8, D=128, ps=16, lens=LENS, window=500, sinks=True)
+    o1, l1 = gh.run(p)
+    rng = np.random.default_rng(3)
+    perm = rng.permutation(p.num_pages)
+    k2 = np.empty_like(p.k_cache)
+    v2 = np.empty_like(p.v_cache)
+    k2[perm] = p.k_cache
+    v2[perm] = p.v_cache
+    bt = p.block_table.copy()
+    used = bt != wl.BT_SENTINEL
+    bt[used] = perm[bt[used]]
+    q = dataclasses.replace(p, k_cache=k2, v_cache=v2, block_table=bt)
+    o2, l2 = gh.run(q)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_interleaved_layout_bitwise():
+    a = _small(41, Hq=16, Hkv=8, D=256, ps=32, lens=LENS, layout="separate")
+    b = _small(41, Hq=16, Hkv=8, D=256, ps=32, lens=LENS, layout="interleaved")
+    oa, la = gh.run(a)
+    ob, lb = gh.run(b)
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+
+
+def test_empty_and_zero_length():
+    p = _small(51, Hq=8, Hkv=2, D=64, ps=16, lens=[0, 5, 0, 40], sinks=True)
+    ref_o, ref_l = oracle.attention(p)
+    out, lse = gh.run(p)
+    gh.assert_parity(out, lse, ref_o, ref_l)
+    p.sinks = None
+    ref_o, ref_l = oracle.attention(p)
+    out, lse = gh.run(p)
+    gh.assert_parity(out, lse, ref_o, ref_l)
+
+
+def test_no_lse_output():
+    p = _small(61, Hq=8, Hkv=2, D=64, ps=16, lens=LENS)
+    ref_o, _ = oracle.attention(p)
+    out, _ = gh.run(p, with_lse=False)
+    gh.assert_parity(out, None, ref_o, None)
+
+
+@pytest.mark.parametrize("cid", [2, 3, 5])
+def test_full_size_configs_sampled(cid):
+    # The benchmark workloads at full size, in the launch configuration the
+    # benchmark uses (planner with host lengths); the oracle evaluates a
+    # sample of rows one by one.
+    p = wl.config_problem(cid)
+    out, lse = gh.run(p)
+    rng = np.random.default_rng(cid)
+    rows = np.unique(np.concatenate([rng.choice(p.batch, size=12, replace=False),
+                                     [int(np.argmax(p.seq_lens)), int(np.argmin(p.seq_lens))]])).astype(np.int32)
+    ref_o, ref_l = oracle.attention(p, rows=rows)
+    gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what=f"config {cid}")
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
