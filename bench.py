@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-KV GQA hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+plan + split-KV decode (stage 1 and LSE merge) on the Llama-3-8B-shaped decode
+workload (B=64, Hq=32, Hkv=8, D=128, page 16, bf16, L~U[512,8192]), then one
+prefix-prefill/extend call on the extend workload (B=8, Hq=32, Hkv=8, D=128,
+page 16, ctx~U[0,4096], q~U[1,2048]).
+
+``value`` is the decode KV-read throughput in TB/s: the algorithmic bytes of
+one decode call (K and V of min(L, window) keys per request and kv head, plus
+q, out, lse and block-table entries) divided by the CUDA-event duration of the
+decode call.  Extend TFLOP/s is reported beside it.  Every step streams more
+than the 129 MB L2 (1.14 GB of decode KV alone) in a fixed order, so no input
+of a step is L2-resident when it starts; L2 is not flushed.
+
+``--impl reference`` times the CPU oracle (the fp64 reference implementation
+of the same attention) on the host cores instead, on a bounded sample of the
+same decode workload per step.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs the same per-GPU
+workload (weak scaling); there is no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DECODE_CFG = 2
+EXTEND_CFG = 4
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return FALLBACK_PEAKS, "fallback"
+
+
+# ---- algorithmic work (per call) -------------------------------------------------
+
+def decode_bytes(p) -> int:
+    """K+V of the attended keys + q + out + lse + block-table entries read."""
+    e = 1 if p.kv_dtype == "fp8_e4m3" else 2
+    L = p.seq_lens.astype(np.int64)
+    n = np.minimum(L, p.window) if p.window > 0 else L
+    kv = int(n.sum()) * p.num_kv_heads * p.head_dim * e * 2
+    B, Hq, D = p.batch, p.num_q_heads, p.head_dim
+    pages = int(((L + p.page_size - 1) // p.page_size).sum())
+    return kv + B * Hq * D * 2 * 2 + B * Hq * 4 + pages * 4
+
+
+def extend_flops(p) -> int:
+    """4 * D * Hq per attended (query, key) pair: Q.K^T and P.V, causal pairs only."""
+    L = p.seq_lens.astype(np.int64)
+    ql = np.diff(p.query_start_loc).astype(np.int64)
+    ctx = L - ql
+    pairs = 0
+    for c, q in zip(ctx, ql):
+        if p.window > 0:
+            i = np.arange(q)
+            pairs += int(np.minimum(c + i + 1, p.window).sum())
+        else:
+            pairs += int(q * c + q * (q + 1) // 2)
+    return 4 * p.head_dim * p.num_q_heads * pairs
+
+
+def kernel_source_hash(files):
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "paged_kv_gqa_12_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, files):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    source is unchanged since it was captured."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not t or t.get("source_hash") != kernel_source_hash(files):
+        return None
+    return t.get("dram_bytes_per_launch")
+
+
+# ---- clocks -----------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampled every 50 ms on a background thread; samples are
+    timestamped on arrival so the timed window can be cut out afterwards."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1 and len(s) >= 8]
+        if not rows:
+            rows = [s for (_, s) in self.samples if len(s) >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][1]),
+                "power_w_max": max((num(r[2]) or 0.0) for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# ---- our arm ------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_gqa_12_gb300 import binding as pb
+    from paged_kv_gqa_12_gb300 import workloads as wl
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pb.load()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def upload(p):
+        def t(a):
+            if a.dtype == np.uint16:
+                return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        return dict(q=t(p.q), k=t(p.k_cache), v=t(p.v_cache), bt=t(p.block_table), sl=t(p.seq_lens),
+                    qsl=None if p.query_start_loc is None else t(p.query_start_loc),
+                    sinks=None if p.sinks is None else t(p.sinks))
+
+    # Weak scaling: each rank holds its own copy of the per-GPU workload.
+    dp = wl.config_problem(DECODE_CFG, batch=args.decode_batch)
+    ep = wl.config_problem(EXTEND_CFG, batch=args.extend_batch)
+    dd, ed = upload(dp), upload(ep)
+    kvd = pb.KV_BF16
+    dplan_kw = dict(mode=pb.MODE_DECODE, num_q_heads=dp.num_q_heads, num_kv_heads=dp.num_kv_heads,
+                    head_dim=dp.head_dim, page_size=dp.page_size, kv_dtype=kvd, max_batch=dp.batch,
+                    max_pages_per_seq=dp.block_table.shape[1], window=dp.window,
+                    has_sinks=dp.sinks is not None, soft_cap=dp.soft_cap)
+    dplan = pb.plan(**dplan_kw, host_seq_lens=dp.seq_lens)
+    dscr = pb.alloc_scratch(dplan, dev)
+    dout = torch.empty(dp.q.shape, dtype=torch.bfloat16, device=dev)
+    dlse = torch.empty(dp.q.shape[:2], dtype=torch.float32, device=dev)
+    extend_ok = args.only != "decode"
+    try:
+        eplan = pb.plan(mode=pb.MODE_EXTEND, num_q_heads=ep.num_q_heads, num_kv_heads=ep.num_kv_heads,
+                        head_dim=ep.head_dim, page_size=ep.page_size, kv_dtype=pb.KV_BF16, max_batch=ep.batch,
+                        max_pages_per_seq=ep.block_table.shape[1], max_total_q=ep.num_rows,
+                        window=ep.window, has_sinks=ep.sinks is not None, soft_cap=ep.soft_cap)
+        escr = pb.alloc_scratch(eplan, dev)
+    except pb.PaError:
+        extend_ok = False
+    decode_on = args.only != "extend"
+    eout = torch.empty(ep.q.shape, dtype=torch.bfloat16, device=dev)
+    else_ = torch.empty(ep.q.shape[:2], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def decode_call():
+        pb.decode(dplan, dd["q"], dd["k"], dd["v"], dd["bt"], dd["sl"], scale=dp.scale, out=dout, lse=dlse,
+                  sinks=dd["sinks"], k_scale=dp.k_scale, v_scale=dp.v_scale, scratch=dscr, stream=stream)
+
+    def extend_call():
+        pb.extend(eplan, ed["q"], ed["k"], ed["v"], ed["bt"], ed["sl"], ed["qsl"], scale=ep.scale, out=eout,
+                  lse=else_, sinks=ed["sinks"], k_scale=ep.k_scale, v_scale=ep.v_scale, scratch=escr,
+                  stream=stream)
+
+    K, W = args.steps, args.warmup
+    for _ in range(W):
+        if decode_on:
+            decode_call()
+        if extend_ok:
+            extend_call()
+    torch.cuda.synchronize(dev)
+    if pb.check(dscr) != 0 or (extend_ok and pb.check(escr) != 0):
+        raise RuntimeError("device error during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    w0 = time.perf_counter()
+    for k in range(K):
+        ev[k][0].record(stream)
+        if decode_on:
+            decode_call()
+        ev[k][1].record(stream)
+        if extend_ok:
+            extend_call()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    loop_s = time.perf_counter() - w0
+    t1 = time.time()
+    if sampler:
+        sampler.stop()
+    dec_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
+    ext_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)] if extend_ok else []
+    if pb.check(dscr) != 0 or (extend_ok and pb.check(escr) != 0):
+        raise RuntimeError("device error during the timed region")
+
+    dec_s, ext_s = sum(dec_ms) / 1e3, sum(ext_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([dec_s, ext_s, loop_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dec_s, ext_s, loop_s = (float(x) for x in t.tolist())
+
+    dbytes = decode_bytes(dp)
+    eflops = extend_flops(ep) if extend_ok else 0
+    value_tbs = world * K * dbytes / max(dec_s, 1e-12) / 1e12
+
+    # ---- end to end through the public API with host buffers ---------------------
+    Ke = min(K, 200)
+    hq = torch.from_numpy(dp.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hbt = torch.from_numpy(dp.block_table).pin_memory()
+    hsl = torch.from_numpy(dp.seq_lens).pin_memory()
+    hout = torch.empty(dp.q.shape, dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty(dp.q.shape[:2], dtype=torch.float32).pin_memory()
+    gq, gbt, gsl = torch.empty_like(dd["q"]), torch.empty_like(dd["bt"]), torch.empty_like(dd["sl"])
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def e2e_step():
+        gq.copy_(hq, non_blocking=True)
+        gbt.copy_(hbt, non_blocking=True)
+        gsl.copy_(hsl, non_blocking=True)
+        plan = pb.plan(**dplan_kw, host_seq_lens=dp.seq_lens)
+        pb.decode(plan, gq, dd["k"], dd["v"], gbt, gsl, scale=dp.scale, out=dout, lse=dlse, sinks=dd["sinks"],
+                  k_scale=dp.k_scale, v_scale=dp.v_scale, scratch=dscr, stream=stream)
+        hout.copy_(dout, non_blocking=True)
+        hlse.copy_(dlse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = hq.numel() * 2 + hbt.numel() * 4 + hsl.numel() * 4
+    d2h = hout.numel() * 2 + hlse.numel() * 4
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    dec_mean = statistics.mean(dec_ms) / 1e3
+    dec_ach = dbytes / dec_mean / 1e9
+    kernels = {
+        "decode": {"bound": "hbm", "achieved": round(dec_ach, 1), "peak": hbm, "unit": "GB/s",
+                   "frac": round(dec_ach / hbm, 4),
+                   "traffic": recorded_traffic("decode_split_kernel", ["decode.cu", "ptx.cuh", "pa_internal.h"]),
+                   "timed": "pa_decode call (split kernel + merge kernel), CUDA events, mean over steps",
+                   "algorithmic_bytes_per_launch": dbytes, "peak_source": f"{peak_src} hbm_gbs"},
+    }
+    if extend_ok:
+        ext_mean = statistics.mean(ext_ms) / 1e3
+        ext_ach = eflops / ext_mean / 1e12
+        kernels["extend"] = {"bound": "tensor", "achieved": round(ext_ach, 2), "peak": bf16, "unit": "TFLOP/s",
+                             "frac": round(ext_ach / bf16, 4),
+                             "traffic": recorded_traffic("extend_kernel", ["extend.cu", "ptx.cuh", "pa_internal.h"]),
+                             "timed": "pa_extend call (scheduler + attention kernel), CUDA events, mean over steps",
+                             "algorithmic_flops_per_launch": eflops, "peak_source": f"{peak_src} bf16_tflops (burst)"}
+    dominant = "decode"
+    if extend_ok and statistics.mean(ext_ms) > statistics.mean(dec_ms):
+        dominant = "extend"
+    roof = {k: v for k, v in kernels[dominant].items() if k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
+    roof["kernel"] = dominant
+
+    cpu = cpu_baseline(dp, args.cpu_sample) if (world == 1 and not args.no_cpu_baseline) else None
+    clocks = sampler.summary(t0, t1) if sampler else None
+    line = {
+        "metric": "paged decode KV-read TB/s (% of HBM peak); extend TFLOP/s (% bf16 peak)",
+        "value": round(value_tbs, 4),
+        "unit": "TB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(loop_s / K * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; N(0,1) values, shuffled page pools)",
+        "config": {"workload": "decode " + wl.CONFIG_NAMES[DECODE_CFG] + " + extend " + wl.CONFIG_NAMES[EXTEND_CFG],
+                   "decode_batch": dp.batch, "decode_tokens": int(dp.seq_lens.sum()),
+                   "extend_batch": ep.batch, "extend_q_rows": ep.num_rows,
+                   "l2": "not flushed: each step streams > 1.2 GB (L2 129 MB) in a fixed order",
+                   "decode_plan": {"tile_tokens": dplan.tile_tokens, "split_tiles": dplan.split_tiles,
+                                   "max_splits": dplan.max_splits, "stages": dplan.stages}},
+        "decode_ms": round(statistics.mean(dec_ms), 4),
+        "extend_ms": round(statistics.mean(ext_ms), 4) if extend_ok else None,
+        "extend_tflops": round(world * K * eflops / ext_s / 1e12, 2) if extend_ok else None,
+        "roofline": roof,
+        "kernels": kernels,
+        "e2e": {"value": round(world * Ke * dbytes / e2e_s / 1e12, 4), "unit": "TB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "what": "decode through the C ABI: pinned-host q/block_table/seq_lens H2D, pa_plan, pa_decode, out/lse D2H"},
+        "gpu_launches": K * ((dplan.launches if decode_on else 0) + (eplan.launches if extend_ok else 0)),
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---- CPU oracle legs --------------------------------------------------------------
+
+def cpu_baseline(p, n_requests: int):
+    """The oracle, as it stands, on a bounded sample of the decode workload:
+    the first n_requests requests (all heads), on all host cores."""
+    import oracle
+    rows = np.arange(min(n_requests, p.batch), dtype=np.int32)
+    cores = os.cpu_count() or 1
+    oracle.attention(p, rows=rows[:1], num_threads=cores)  # load + warm
+    t = time.perf_counter()
+    oracle.attention(p, rows=rows, num_threads=cores)
+    dt = time.perf_counter() - t
+    sub = sample_bytes(p, rows)
+    return {"value": round(sub / dt / 1e12, 9), "unit": "TB/s", "cores": cores, "kind": "oracle",
+            "seconds": round(dt, 3),
+            "sample": f"decode requests 0..{len(rows) - 1} of the same workload (all {p.num_q_heads} heads), "
+                      f"{sub} algorithmic bytes"}
+
+
+def sample_bytes(p, rows):
+    import dataclasses
+    sub = dataclasses.replace(p, q=p.q[rows], seq_lens=p.seq_lens[rows], block_table=p.block_table[rows])
+    return decode_bytes(sub)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_gqa_12_gb300 import workloads as wl
+    p = wl.config_problem(DECODE_CFG)
+    cores = os.cpu_count() or 1
+    K, W = args.steps, args.warmup
+    # bounded per-step sample: one request (all heads) per step, cycling
+    times, nbytes = [], 0
+    for k in range(W + K):
+        r = np.array([k % p.batch], np.int32)
+        t = time.perf_counter()
+        oracle.attention(p, rows=r, num_threads=cores)
+        dt = time.perf_counter() - t
+        if k >= W:
+            times.append(dt)
+            nbytes += sample_bytes(p, r)
+    tot = sum(times)
+    value = nbytes / tot / 1e12
+    line = {"impl": "reference", "metric": "paged decode KV-read TB/s (% of HBM peak); extend TFLOP/s (% bf16 peak)",
+            "value": value, "unit": "TB/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": K,
+            "warmup": W, "ms_per_step": tot / K * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": "decode " + wl.CONFIG_NAMES[DECODE_CFG]},
+            "cpu_baseline": {"value": value, "unit": "TB/s", "cores": cores, "kind": "oracle",
+                             "sample": "one decode request (all heads) per step, cycling through the batch"},
+            "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-sample", type=int, default=64, help="decode requests in the CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["decode", "extend"], default=None,
+                    help="run one of the two calls per step (profiling of reduced cases)")
+    ap.add_argument("--decode-batch", type=int, default=None, help="keep the first N decode requests")
+    ap.add_argument("--extend-batch", type=int, default=None, help="keep the first N extend requests")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -100,7 +100,8 @@ typedef struct {
   int32_t smem_bytes;         /* dynamic shared memory per CTA */
   int32_t grid[3];            /* main kernel grid */
   int64_t scratch_bytes;      /* device scratch the calls need (>= 256) */
-  int32_t reserved[8];
+  int32_t launches;           /* kernel launches one call makes */
+  int32_t reserved[7];
 } pa_plan_t;
 
 /* Plan a decode or extend call from capacities.  host_seq_lens (host memory,

@@ -61,7 +61,8 @@ class PaPlan(ctypes.Structure):
         ("smem_bytes", ctypes.c_int32),
         ("grid", ctypes.c_int32 * 3),
         ("scratch_bytes", ctypes.c_int64),
-        ("reserved", ctypes.c_int32 * 8),
+        ("launches", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 7),
     ]
 
 

@@ -108,6 +108,7 @@ pa_status plan_decode(const pa_shape& s, const int32_t* host_lens, int32_t batch
   out->grid[2] = s.max_batch;
   const int64_t rows = static_cast<int64_t>(s.max_batch) * s.num_q_heads * max_splits;
   out->scratch_bytes = kScratchHeaderBytes + align_up(rows * s.head_dim * 4, 256) + align_up(rows * 4, 256);
+  out->launches = 2;  // split kernel + merge kernel
   return PA_OK;
 }
 

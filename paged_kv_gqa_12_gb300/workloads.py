@@ -230,41 +230,43 @@ CONFIG_NAMES = {
 }
 
 
-def config_problem(cid: int, seed: int | None = None, **kw) -> Problem:
+def config_problem(cid: int, seed: int | None = None, batch: int | None = None, **kw) -> Problem:
     """The five workloads: shapes, distributions and options as specified for
-    each benchmark configuration; seed defaults to 1000 + config id."""
+    each benchmark configuration; seed defaults to 1000 + config id.
+    ``batch`` keeps only the first requests (same draws), for reduced cases."""
     seed = 1000 + cid if seed is None else seed
     rng = np.random.default_rng(seed + 7919)
     name = CONFIG_NAMES[cid]
+    cut = slice(None) if batch is None else slice(0, batch)
     if cid == 1:
         B = 4
-        sl = rng.integers(1, 301, size=B)
+        sl = rng.integers(1, 301, size=B)[cut]
         args = dict(num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=16,
                     seq_lens=sl, scale=64 ** -0.5, pool_pages=128)
         return build_problem("decode", seed=seed, name=name, **{**args, **kw})
     if cid == 2:
         B = 64
-        sl = rng.integers(512, 8193, size=B)
+        sl = rng.integers(512, 8193, size=B)[cut]
         args = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
                     seq_lens=sl, scale=128 ** -0.5)
         return build_problem("decode", seed=seed, name=name, **{**args, **kw})
     if cid == 3:
         B = 128
-        sl = np.floor(np.exp(rng.uniform(math.log(1024), math.log(32768), size=B))).astype(np.int64)
+        sl = np.floor(np.exp(rng.uniform(math.log(1024), math.log(32768), size=B))).astype(np.int64)[cut]
         args = dict(num_q_heads=64, num_kv_heads=8, head_dim=64, page_size=64,
                     seq_lens=sl, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05,
                     window=1024, sinks=True, scale=64 ** -0.5)
         return build_problem("decode", seed=seed, name=name, **{**args, **kw})
     if cid == 4:
         B = 8
-        ctx = rng.integers(0, 4097, size=B)
-        ql = rng.integers(1, 2049, size=B)
+        ctx = rng.integers(0, 4097, size=B)[cut]
+        ql = rng.integers(1, 2049, size=B)[cut]
         args = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
                     seq_lens=ctx + ql, query_lens=ql, scale=128 ** -0.5)
         return build_problem("extend", seed=seed, name=name, **{**args, **kw})
     if cid == 5:
         B = 256
-        sl = np.clip(np.rint(rng.lognormal(math.log(2048), 1.0, size=B)), 1, 65536).astype(np.int64)
+        sl = np.clip(np.rint(rng.lognormal(math.log(2048), 1.0, size=B)), 1, 65536).astype(np.int64)[cut]
         args = dict(num_q_heads=16, num_kv_heads=8, head_dim=256, page_size=32,
                     seq_lens=sl, soft_cap=50.0, window=4096, scale=256 ** -0.5)
         return build_problem("decode", seed=seed, name=name, **{**args, **kw})
