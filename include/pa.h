@@ -142,6 +142,33 @@ pa_status pa_decode(const pa_plan_t* plan,
                     float* lse,
                     void* scratch, int64_t scratch_bytes, void* stream);
 
+/* pa_decode without a caller-provided workspace.  The source pages have no
+ * counterpart to this entry point; it exists for callers that cannot allocate
+ * device memory for a scratch buffer -- for example a plugin or host runtime
+ * with no device allocator of its own, a process whose memory pool already
+ * owns the whole GPU, or code that must never allocate so that its latency
+ * stays fixed.  Arguments and results are those of pa_decode, minus scratch.
+ *   - The workspace is a 16 MiB array inside the library's device image,
+ *     present on every GPU that loads the library until the process exits.
+ *     Plans whose scratch_bytes exceed 16 MiB return PA_ERR_SCRATCH_TOO_SMALL.
+ *   - The first call on each device looks up the array's device address (a
+ *     runtime query, no allocation); make that first call before any stream
+ *     capture.  Nothing is allocated, by this call or any later one.
+ *   - Every call on a device shares the one array and clears its error header
+ *     first; calls that overlap on the GPU race on it, so the caller must
+ *     serialise them.  Device-side error codes are not reported here; use
+ *     pa_decode with pa_check when they are needed. */
+pa_status pa_decode_static_scratch(const pa_plan_t* plan,
+                                   const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                                   const void* k_cache, const void* v_cache,
+                                   int64_t kv_stride_page, int64_t kv_stride_tok, int64_t kv_stride_head,
+                                   int32_t num_pages,
+                                   const int32_t* block_table, int64_t bt_stride,
+                                   const int32_t* seq_lens, int32_t batch,
+                                   float scale, const float* sinks, float k_scale, float v_scale,
+                                   void* out, int64_t out_stride_tok, int64_t out_stride_head,
+                                   float* lse, void* stream);
+
 /* Prefix-prefill / extend over the paged cache (all keys, cached and new,
  * are read from the pages).
  *   q               device bf16 [total_q, Hq, D] (strides as for decode)

@@ -27,7 +27,7 @@ KV_BF16 = 0
 KV_FP8_E4M3 = 1
 
 EXPORTED_SYMBOLS = ("pa_plan", "pa_decode", "pa_extend", "pa_scratch_init", "pa_check",
-                    "pa_status_string", "pa_version")
+                    "pa_status_string", "pa_version", "pa_decode_static_scratch")
 
 
 class PaShape(ctypes.Structure):
@@ -94,6 +94,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.pa_extend.argtypes = [ctypes.POINTER(PaPlan), vp, i64, i64, vp, vp, i64, i64, i64, i32, vp, i64,
                             vp, vp, i32, i32, f32, vp, f32, f32, vp, i64, i64, vp, vp, i64, vp]
     L.pa_extend.restype = ctypes.c_int
+    L.pa_decode_static_scratch.argtypes = [ctypes.POINTER(PaPlan), vp, i64, i64, vp, vp, i64, i64, i64, i32,
+                                           vp, i64, vp, i32, f32, vp, f32, f32, vp, i64, i64, vp, vp]
+    L.pa_decode_static_scratch.restype = ctypes.c_int
     L.pa_scratch_init.argtypes = [vp, vp]
     L.pa_scratch_init.restype = ctypes.c_int
     L.pa_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -175,6 +178,20 @@ def extend(p: PaPlan, q, k_cache, v_cache, block_table, seq_lens, query_start_lo
         out.stride(0), out.stride(1), _ptr(lse), _ptr(scratch), scratch.numel() * scratch.element_size(),
         _stream(stream))
     _check(status, "pa_extend")
+
+
+def decode_static_scratch(p: PaPlan, q, k_cache, v_cache, block_table, seq_lens, *, scale: float, out,
+                          lse=None, sinks=None, k_scale: float = 1.0, v_scale: float = 1.0, stream=None):
+    """pa_decode_static_scratch: decode for callers that cannot allocate a
+    workspace; the library's own fixed 16 MiB device array is used instead
+    (calls on one device must not overlap)."""
+    sp, st, sh = _kv_strides(k_cache, v_cache)
+    status = load().pa_decode_static_scratch(
+        ctypes.byref(p), _ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), sp, st, sh,
+        k_cache.shape[0], _ptr(block_table), block_table.stride(0), _ptr(seq_lens), seq_lens.shape[0],
+        float(scale), _ptr(sinks), float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1),
+        _ptr(lse), _stream(stream))
+    _check(status, "pa_decode_static_scratch")
 
 
 def scratch_init(scratch, stream=None):
