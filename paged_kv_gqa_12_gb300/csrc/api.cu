@@ -40,6 +40,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+}  // namespace
+
 pa_status validate_shape(const pa_shape& s) {
   if (s.mode != PA_MODE_DECODE && s.mode != PA_MODE_EXTEND) return PA_ERR_INVALID_ARG;
   if (s.num_q_heads <= 0 || s.num_kv_heads <= 0 || s.num_q_heads % s.num_kv_heads != 0) return PA_ERR_INVALID_ARG;
@@ -55,6 +57,8 @@ pa_status validate_shape(const pa_shape& s) {
   if (static_cast<int64_t>(s.max_pages_per_seq) * s.page_size > (int64_t{1} << 30)) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
+
+namespace {
 
 // Attended keys of one decode request: min(L, W) (W = 0: off).
 int64_t decode_keys(int64_t L, int window) { return window > 0 ? std::min<int64_t>(L, window) : L; }
@@ -112,6 +116,8 @@ pa_status plan_decode(const pa_shape& s, const int32_t* host_lens, int32_t batch
   return PA_OK;
 }
 
+}  // namespace
+
 // 4-D tensor map over a paged cache [pages, page_size, kv_heads, head_dim]:
 // dims (innermost first) head_dim, kv head, slot, page.  Box: `box_bytes`
 // of head_dim, one head, `box_rows` slots, one page, swizzled so that the
@@ -136,6 +142,23 @@ pa_status make_kv_map(CUtensorMap* map, const void* base, bool fp8, int D, int H
   return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
 }
 
+// 3-D tensor map over packed queries [rows, Hq, D] (bf16): dims head_dim,
+// q head, row; box 64 dims x `group` heads x `rows_per_box` rows, 128-byte
+// swizzle, so one box per 64-dim chunk lands as a [rows*group, 64] K-major tile.
+pa_status make_q_map(CUtensorMap* map, const void* base, int D, int Hq, int rows, int64_t st_tok, int64_t st_head,
+                     int group, int rows_per_box) {
+  auto fn = encode_fn();
+  if (!fn) return PA_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(st_head * 2), static_cast<cuuint64_t>(st_tok * 2)};
+  cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(rows_per_box)};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PA_OK : PA_ERR_UNSUPPORTED;
+}
+
 pa_status check_kv(const pa_shape& s, const void* k, const void* v, int64_t st_page, int64_t st_tok,
                    int64_t st_head, int32_t num_pages) {
   if (!k || !v || num_pages <= 0) return PA_ERR_INVALID_ARG;
@@ -145,6 +168,8 @@ pa_status check_kv(const pa_shape& s, const void* k, const void* v, int64_t st_p
   if ((st_page * e) % 16 || (st_tok * e) % 16 || (st_head * e) % 16) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
+
+namespace {
 
 pa_status check_rows(const void* p, int64_t st_tok, int64_t st_head, bool required) {
   if (!p) return required ? PA_ERR_INVALID_ARG : PA_OK;

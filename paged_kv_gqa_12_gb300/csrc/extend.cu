@@ -1,18 +1,525 @@
-// Prefix-prefill / extend over the paged cache (placeholder until the
-// tensor-core kernel lands).
+// Prefix-prefill / extend over the paged KV cache on the 5th-generation tensor
+// cores (tcgen05, TMEM accumulators, TMA operand loads).
+//
+// Operation: "vllm/attention/ops/prefix_prefill.py", context_attention_fwd /
+// _fwd_kernel: query i of request b sits at sequence position
+// ctx_b + i (ctx_b = seq_len - query_len) and attends to every key j <= its
+// position (the cached context unmasked, the new tokens causally), within the
+// sliding window when one is set; all keys are read from the pages, as in the
+// b12x backend ("vllm/v1/attention/backends/b12x", forward), where the new
+// tokens are appended before attention runs.
+//
+// Design (GB300):
+//   * Tile = 128 query rows x one kv head: the G q heads of each token are
+//     packed into the MMA M dimension (row = token * G + head), so one K/V
+//     tile feeds all heads that share it.
+//   * Warp roles in a 256-thread CTA: warp 0 issues TMA (Q once; per key tile
+//     one box per page for K and V, page ids from the block table), warp 1
+//     allocates TMEM and issues tcgen05.mma from one thread, warps 4-7 run
+//     the softmax with one TMEM lane (= one query row) per thread.
+//   * S = Q K^T (M=128, N=BN keys) lands in one of two TMEM buffers, so the
+//     next tile's QK overlaps this tile's softmax; P (bf16) is written back
+//     over S and consumed from TMEM by O += P V (V read MN-major from shared
+//     memory); O stays in TMEM for the whole key loop.
+//   * Online softmax in the log2 domain with lazy rescaling: O and l are
+//     rescaled only when the row maximum grows by more than 2^8, which is
+//     exact because the final normalisation uses the same stale maximum.
+//   * Key tiles wholly outside [first key of the window, last query] are not
+//     visited; pages outside [window start, sequence end) are fetched as
+//     out-of-bounds TMA boxes (zero fill), and value rows past the sequence end
+//     inside the last page are zeroed, so stale or NaN slots never meet P = 0.
+//   * A one-CTA scheduler kernel builds the (request, query tile) list from
+//     the device metadata, heaviest first; CTA i takes item i / Hkv.
+#include <climits>
+#include <cstdint>
+
 #include "extend.h"
 #include "pa_internal.h"
+#include "tcgen05.cuh"
 
 namespace pa {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kRows = 128;           // MMA M: query rows per tile
+constexpr int kSchedThreads = 1024;
+constexpr int kBuckets = 256;        // work classes for the longest-first order
+constexpr int kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+
+struct ExtendParams {
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int batch, total_q, num_q_heads, num_kv_heads, group, page_size, num_pages;
+  int tm;                 // tokens per tile (128 / group, rounded down)
+  int max_kv;             // capacity: keys per request
+  int block_n;            // keys per tile
+  float scale_log2, cap_log2, scale_over_cap;
+  int window;
+  const float* sinks;
+  uint16_t* out;
+  int64_t out_stride_tok, out_stride_head;
+  float* lse;
+  int2* work;
+  int* work_count;
+  int work_cap;
+  uint32_t* err;
+};
+
+// Key tiles an item touches (its cost), from the rows it holds.
+__device__ __forceinline__ bool item_range(const ExtendParams& p, int b, int mt, int& qs, int& qlen, int& ctx,
+                                           int& t0, int& t_end, int& lo_min, int& kt0, int& n_tiles) {
+  qs = p.qsl[b];
+  qlen = p.qsl[b + 1] - qs;
+  const int L = p.seq_lens[b];
+  ctx = L - qlen;
+  t0 = mt * p.tm;
+  if (qlen <= 0 || ctx < 0 || L > p.max_kv || qs < 0 || qs + qlen > p.total_q || t0 >= qlen) return false;
+  t_end = min(qlen, t0 + p.tm);
+  const int pos_min = ctx + t0;
+  const int pos_max = ctx + t_end - 1;
+  lo_min = p.window > 0 ? max(0, pos_min - p.window + 1) : 0;
+  kt0 = lo_min / p.block_n;
+  n_tiles = pos_max / p.block_n - kt0 + 1;
+  return true;
+}
+
+__global__ void __launch_bounds__(kSchedThreads) extend_schedule_kernel(const ExtendParams p) {
+  __shared__ int s_hist[kBuckets];
+  __shared__ int s_off[kBuckets];
+  __shared__ int s_total;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kBuckets; i += kSchedThreads) s_hist[i] = 0;
+  if (tid == 0) s_total = 0;
+  __syncthreads();
+  const int per = (p.batch + kSchedThreads - 1) / kSchedThreads;
+  const int b0 = min(p.batch, tid * per);
+  const int b1 = min(p.batch, b0 + per);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int qlen = p.qsl[b + 1] - p.qsl[b];
+    if (qlen <= 0) continue;
+    const int nmt = (qlen + p.tm - 1) / p.tm;
+    for (int mt = 0; mt < nmt; ++mt) {
+      int qs, ql, ctx, t0, te, lo, kt0, n;
+      if (!item_range(p, b, mt, qs, ql, ctx, t0, te, lo, kt0, n)) {
+        atomicOr(p.err, kErrCapacity);
+        continue;
+      }
+      atomicAdd(&s_hist[min(n, kBuckets - 1)], 1);
+      ++local;
+    }
+  }
+  atomicAdd(&s_total, local);
+  __syncthreads();
+  // descending exclusive scan: heaviest class first (one warp, 8 classes per lane)
+  if (tid < 32) {
+    constexpr int per_lane = kBuckets / 32;
+    int vals[per_lane];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < per_lane; ++i) {
+      vals[i] = s_hist[kBuckets - 1 - (tid * per_lane + i)];
+      sum += vals[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (tid >= off) incl += v;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < per_lane; ++i) {
+      s_off[kBuckets - 1 - (tid * per_lane + i)] = run;
+      run += vals[i];
+    }
+  }
+  __syncthreads();
+  for (int b = b0; b < b1; ++b) {
+    const int qlen = p.qsl[b + 1] - p.qsl[b];
+    if (qlen <= 0) continue;
+    const int nmt = (qlen + p.tm - 1) / p.tm;
+    for (int mt = 0; mt < nmt; ++mt) {
+      int qs, ql, ctx, t0, te, lo, kt0, n;
+      if (!item_range(p, b, mt, qs, ql, ctx, t0, te, lo, kt0, n)) continue;
+      const int pos = atomicAdd(&s_off[min(n, kBuckets - 1)], 1);
+      if (pos < p.work_cap) p.work[pos] = make_int2(b, mt);
+    }
+  }
+  if (tid == 0) {
+    int total = s_total;
+    if (total > p.work_cap) {
+      atomicOr(p.err, kErrSchedOverflow);
+      total = p.work_cap;
+    }
+    *p.work_count = total;
+  }
+}
+
+// Bounded wait that also gives up as soon as any CTA has reported an error,
+// so one failure cannot make every later CTA wait out its own timeout.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 255u) == 0 && *reinterpret_cast<volatile uint32_t*>(err) != 0u) return false;
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+      atomicOr(err, kErrWaitTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+template <int D, int BN, int NST>
+struct ExtTraits {
+  static constexpr int NCH = D / 64;                 // 128-byte column chunks per row
+  static constexpr int Q_CHUNK = kRows * 128;        // 16 KB
+  static constexpr int Q_BYTES = NCH * Q_CHUNK;
+  static constexpr int KV_CHUNK = BN * 128;
+  static constexpr int TILE = NCH * KV_CHUNK;        // K (or V) tile
+  static constexpr int STAGE = 2 * TILE;
+  static constexpr int SMEM_DATA = Q_BYTES + NST * STAGE;
+  static constexpr int SMEM = 1024 + SMEM_DATA + 256;
+  static constexpr uint32_t TMEM_O = 256;            // O columns start
+  static_assert(2 * BN <= 256 && D <= 256, "TMEM plan: two S buffers in [0,256), O in [256,512)");
+  static_assert(BN % 64 == 0, "P is stored 32 columns (64 keys) at a time");
+};
+
+template <int D, int BN, int NST>
+__global__ void __launch_bounds__(kThreads, 1)
+extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv, const ExtendParams p) {
+  using T = ExtTraits<D, BN, NST>;
+  const int idx = blockIdx.x / p.num_kv_heads;
+  const int kvh = blockIdx.x - idx * p.num_kv_heads;
+  if (idx >= *p.work_count) return;
+  // another CTA already failed: leave (CTA-uniform, before any TMEM allocation)
+  if (__syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<volatile uint32_t*>(p.err) != 0u)) return;
+  const int2 item = p.work[idx];
+  const int b = item.x;
+  int qs, qlen, ctx, t0, t_end, lo_min, kt0, n;
+  if (!item_range(p, b, item.y, qs, qlen, ctx, t0, t_end, lo_min, kt0, n)) return;
+  const int L = ctx + qlen;
+  const int G = p.group;
+  const int ps = p.page_size;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_s = smem;
+  uint8_t* kv_s = smem + T::Q_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::SMEM_DATA);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = kv_full + NST;
+  uint64_t* s_full = kv_empty + NST;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_done = p_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 2);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (tid == 0) {
+    prefetch_tensormap(&tmq);
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+    mbar_init(q_full, 1);
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&o_done[i], 1);
+    }
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+    bool ok = true;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(T::NCH * p.tm * G * 128));
+#pragma unroll
+      for (int c = 0; c < T::NCH; ++c) tma_load_3d(q_s + c * T::Q_CHUNK, &tmq, c * 64, kvh * G, qs + t0, q_full);
+    }
+    const int npg = BN / ps;
+    for (int j = 0; j < n && ok; ++j) {
+      const int stage = j % NST;
+      if (j >= NST) ok = __all_sync(0xffffffffu, wait_or_abort(&kv_empty[stage], ((j / NST) - 1) & 1, p.err));
+      if (!ok) break;
+      if (lane == 0) mbar_arrive_expect_tx(&kv_full[stage], static_cast<uint32_t>(T::STAGE));
+      __syncwarp();
+      if (lane < npg) {
+        const int k0 = (kt0 + j) * BN;
+        const int pg = k0 / ps + lane;
+        // pages with no attended key are fetched out of bounds: TMA writes zeros
+        const bool outside = (pg * ps >= L) || ((pg + 1) * ps <= lo_min);
+        const int coord = outside ? p.num_pages : bt_row[pg];
+        uint8_t* ks = kv_s + stage * T::STAGE;
+        uint8_t* vs = ks + T::TILE;
+#pragma unroll
+        for (int c = 0; c < T::NCH; ++c) {
+          const int dst = c * T::KV_CHUNK + lane * ps * 128;
+          tma_load_4d(ks + dst, &tmk, c * 64, kvh, 0, coord, &kv_full[stage]);
+          tma_load_4d(vs + dst, &tmv, c * 64, kvh, 0, coord, &kv_full[stage]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (one thread) ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16(kRows, BN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(kRows, D, false, true);
+      const uint32_t q_u = smem_u32(q_s);
+      const uint32_t kv_u = smem_u32(kv_s);
+      bool ok = wait_or_abort(q_full, 0, p.err);
+      tc_fence_after();
+      for (int j = 0; j <= n && ok; ++j) {
+        if (j < n) {
+          const int stage = j % NST;
+          ok = wait_or_abort(&kv_full[stage], (j / NST) & 1, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t tS = tbase + static_cast<uint32_t>((j & 1) * BN);
+          const uint32_t k_u = kv_u + stage * T::STAGE;
+#pragma unroll
+          for (int s = 0; s < D / 16; ++s) {
+            const uint64_t ad = sdesc_sw128(q_u + (s >> 2) * T::Q_CHUNK + (s & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(k_u + (s >> 2) * T::KV_CHUNK + (s & 3) * 32, 16, 1024);
+            umma_ss(tS, ad, bd, idesc_qk, s > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[j & 1]);
+        }
+        if (j >= 1) {
+          const int jj = j - 1;
+          const int st = jj % NST;
+          ok = wait_or_abort(&p_full[jj & 1], (jj >> 1) & 1, p.err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t tP = tbase + static_cast<uint32_t>((jj & 1) * BN);
+          const uint32_t v_u = kv_u + st * T::STAGE + T::TILE;
+#pragma unroll
+          for (int s = 0; s < BN / 16; ++s) {
+            const uint64_t bd = sdesc_sw128(v_u + s * 16 * 128, T::KV_CHUNK, 1024);
+            umma_ts(tbase + T::TMEM_O, tP + s * 8, bd, idesc_pv, (jj > 0 || s > 0) ? 1u : 0u);
+          }
+          umma_commit(&o_done[jj & 1]);
+          umma_commit(&kv_empty[st]);
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- softmax warpgroup: one query row per thread ----------------
+    const int wq = warp - 4;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const int tok = t0 + r / G;
+    const int hh = r - (r / G) * G;
+    const bool row_ok = (r < p.tm * G) && (tok < qlen);
+    const int pos = ctx + min(tok, t_end - 1);
+    const int lo = p.window > 0 ? pos - p.window + 1 : INT_MIN / 2;
+    const bool capped = p.cap_log2 > 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const int k0 = (kt0 + j) * BN;
+      ok = __all_sync(0xffffffffu, wait_or_abort(&s_full[j & 1], (j >> 1) & 1, p.err));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tS = tbase + lane_off + static_cast<uint32_t>((j & 1) * BN);
+      uint32_t sr[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+      tmem_wait_ld();
+      const bool full = (k0 >= lo) && (k0 + BN - 1 <= pos);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < BN; ++i) {
+        float v = __uint_as_float(sr[i]);
+        v = capped ? p.cap_log2 * tanhf(v * p.scale_over_cap) : v * p.scale_log2;
+        if (!full && (k0 + i > pos || k0 + i < lo)) v = -INFINITY;
+        sr[i] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      const float m_new = fmaxf(m_run, mx);
+      const bool need = m_new > m_run + kRescaleThreshold;
+      const bool any_need = __any_sync(0xffffffffu, need);
+      const float m_use = need ? m_new : m_run;
+      const float m_base = (m_use == -INFINITY) ? 0.f : m_use;
+      const float alpha = (m_use == m_run || m_use == -INFINITY) ? 1.f : ex2(m_run - m_use);
+      float ls = 0.f;
+      uint32_t pk[BN / 2];
+#pragma unroll
+      for (int i = 0; i < BN / 2; ++i) {
+        const float p0 = ex2(__uint_as_float(sr[2 * i]) - m_base);
+        const float p1 = ex2(__uint_as_float(sr[2 * i + 1]) - m_base);
+        ls += p0 + p1;
+        pk[i] = pack_bf16x2(p0, p1);
+      }
+      l_run = l_run * alpha + ls;
+      m_run = m_use;
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c) tmem_st32(tS + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
+      tmem_wait_st();
+      if (any_need && j > 0) {
+        // O must hold PV of tile j-1 before it is rescaled (and no PV may run meanwhile)
+        ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.err));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tO = tbase + lane_off + T::TMEM_O;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tO + c * 32, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          tmem_st32(tO + c * 32, u);
+        }
+        tmem_wait_st();
+      }
+      // value rows past the sequence end inside the last page of this tile
+      const int pend = min(k0 + BN, ((L + ps - 1) / ps) * ps);
+      if (L < pend) {
+        uint8_t* vs = kv_s + (j % NST) * T::STAGE + T::TILE;
+        const int nrows = pend - L;
+        const int units = nrows * T::NCH * 8;   // 16-byte units
+        for (int u = r; u < units; u += kRows) {
+          const int row = (L - k0) + u / (T::NCH * 8);
+          const int c = (u / 8) % T::NCH;
+          *reinterpret_cast<uint4*>(vs + c * T::KV_CHUNK + row * 128 + (u & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[j & 1]);
+    }
+    if (ok && n > 0) ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, p.err));
+    if (ok) {
+      tc_fence_after();
+      const int hq = kvh * G + hh;
+      float M2 = m_run, f = 1.f, Z = l_run;
+      if (p.sinks != nullptr) {
+        const float sk = p.sinks[hq] * kLog2e;
+        M2 = fmaxf(m_run, sk);
+        f = (m_run == -INFINITY) ? 0.f : ex2(m_run - M2);
+        Z = l_run * f + ex2(sk - M2);
+      }
+      const float inv = (Z > 0.f) ? f / Z : 0.f;
+      const int64_t orow = static_cast<int64_t>(qs + min(tok, qlen - 1));
+      uint16_t* op = p.out + orow * p.out_stride_tok + static_cast<int64_t>(hq) * p.out_stride_head;
+      const uint32_t tO = tbase + lane_off + T::TMEM_O;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tO + c * 32, u);
+        tmem_wait_ld();
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(op + c * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(u[8 * v + 0]) * inv, __uint_as_float(u[8 * v + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(u[8 * v + 2]) * inv, __uint_as_float(u[8 * v + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(u[8 * v + 4]) * inv, __uint_as_float(u[8 * v + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(u[8 * v + 6]) * inv, __uint_as_float(u[8 * v + 7]) * inv);
+            dst[v] = w;
+          }
+        }
+      }
+      if (row_ok && p.lse != nullptr) {
+        p.lse[orow * p.num_q_heads + hq] = (Z > 0.f) ? (M2 + lg2(Z)) * kLn2 : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tbase, kTmemCols);
+}
+
+template <int D, int BN, int NST>
+cudaError_t launch_ext(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                       const ExtendParams& p, cudaStream_t stream) {
+  using T = ExtTraits<D, BN, NST>;
+  extend_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  auto kern = extend_attn_kernel<D, BN, NST>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
+  if (e != cudaSuccess) return e;
+  const int64_t blocks = static_cast<int64_t>(p.work_cap) * p.num_kv_heads;
+  kern<<<static_cast<unsigned>(blocks), kThreads, T::SMEM, stream>>>(tmq, tmk, tmv, p);
+  return cudaGetLastError();
+}
+
+// Per head_dim: keys per tile and pipeline stages (shared memory <= 227 KB).
+struct ExtChoice {
+  int block_n, stages, smem;
+};
+
+ExtChoice ext_choice(int D) {
+  if (D == 64) return {128, 4, ExtTraits<64, 128, 4>::SMEM};
+  if (D == 128) return {128, 2, ExtTraits<128, 128, 2>::SMEM};
+  return {64, 2, ExtTraits<256, 64, 2>::SMEM};
+}
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
 
 pa_status plan_extend(const pa_shape& s, int num_sms, pa_plan_t* out) {
-  (void)s;
   (void)num_sms;
-  (void)out;
-  return PA_ERR_UNSUPPORTED;
+  if (s.kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
+  const int G = s.num_q_heads / s.num_kv_heads;
+  const int tm = kRows / G;
+  const ExtChoice ch = ext_choice(s.head_dim);
+  const int64_t work_cap = (static_cast<int64_t>(s.max_total_q) + tm - 1) / tm + s.max_batch;
+  if (work_cap * s.num_kv_heads > INT32_MAX) return PA_ERR_UNSUPPORTED;
+  out->tile_tokens = ch.block_n;
+  out->split_tiles = tm;
+  out->max_splits = 1;
+  out->stages = ch.stages;
+  out->warps = kThreads / 32;
+  out->bt_cache = 0;
+  out->smem_bytes = ch.smem;
+  out->grid[0] = static_cast<int32_t>(work_cap * s.num_kv_heads);
+  out->grid[1] = 1;
+  out->grid[2] = 1;
+  out->scratch_bytes = kScratchHeaderBytes + align_up(work_cap * 8, 256);
+  out->launches = 2;  // scheduler + attention kernel
+  return PA_OK;
 }
 
 }  // namespace pa
+
+using namespace pa;
+
+namespace {
+
+constexpr float kLog2eHost = 1.4426950408889634f;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
 
 extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_stride_tok, int64_t q_stride_head,
                                const void* k_cache, const void* v_cache, int64_t kv_stride_page,
@@ -22,5 +529,82 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
                                const float* sinks, float k_scale, float v_scale, void* out, int64_t out_stride_tok,
                                int64_t out_stride_head, float* lse, void* scratch, int64_t scratch_bytes,
                                void* stream) {
-  return PA_ERR_UNSUPPORTED;
+  (void)k_scale;
+  (void)v_scale;
+  if (!plan) return PA_ERR_INVALID_ARG;
+  const pa_shape& s = plan->shape;
+  if (s.mode != PA_MODE_EXTEND || validate_shape(s) != PA_OK) return PA_ERR_INVALID_ARG;
+  if (s.kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
+  if (batch < 0 || batch > s.max_batch || total_q < 0 || total_q > s.max_total_q) return PA_ERR_INVALID_ARG;
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PA_ERR_INVALID_ARG;
+  if ((sinks != nullptr) != (s.has_sinks != 0)) return PA_ERR_INVALID_ARG;
+  if (!scratch) return PA_ERR_INVALID_ARG;
+  if (scratch_bytes < plan->scratch_bytes) return PA_ERR_SCRATCH_TOO_SMALL;
+  if ((reinterpret_cast<uintptr_t>(scratch) & 255u) != 0) return PA_ERR_UNSUPPORTED;
+  if (batch == 0 || total_q == 0) return PA_OK;
+  if (!q || !out || !block_table || !seq_lens || !query_start_loc || bt_stride < 0) return PA_ERR_INVALID_ARG;
+  if (q_stride_tok <= 0 || q_stride_head <= 0 || out_stride_tok <= 0 || out_stride_head <= 0)
+    return PA_ERR_INVALID_ARG;
+  // q feeds a TMA tensor map and out is written in 16-byte vectors
+  if (!aligned16(q) || !aligned16(out) || (q_stride_tok % 8) || (q_stride_head % 8) || (out_stride_tok % 8) ||
+      (out_stride_head % 8))
+    return PA_ERR_UNSUPPORTED;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return PA_ERR_UNSUPPORTED;
+  pa_status st = check_kv(s, k_cache, v_cache, kv_stride_page, kv_stride_tok, kv_stride_head, num_pages);
+  if (st != PA_OK) return st;
+
+  const int G = s.num_q_heads / s.num_kv_heads;
+  const int tm = kRows / G;
+  const ExtChoice ch = ext_choice(s.head_dim);
+  CUtensorMap tmq, tmk, tmv;
+  if ((st = make_q_map(&tmq, q, s.head_dim, s.num_q_heads, total_q, q_stride_tok, q_stride_head, G, tm)) !=
+      PA_OK)
+    return st;
+  if ((st = make_kv_map(&tmk, k_cache, false, s.head_dim, s.num_kv_heads, s.page_size, num_pages,
+                               kv_stride_page, kv_stride_tok, kv_stride_head, s.page_size)) != PA_OK)
+    return st;
+  if ((st = make_kv_map(&tmv, v_cache, false, s.head_dim, s.num_kv_heads, s.page_size, num_pages,
+                               kv_stride_page, kv_stride_tok, kv_stride_head, s.page_size)) != PA_OK)
+    return st;
+
+  ExtendParams p{};
+  p.seq_lens = seq_lens;
+  p.qsl = query_start_loc;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.batch = batch;
+  p.total_q = total_q;
+  p.num_q_heads = s.num_q_heads;
+  p.num_kv_heads = s.num_kv_heads;
+  p.group = G;
+  p.page_size = s.page_size;
+  p.num_pages = num_pages;
+  p.tm = tm;
+  p.max_kv = s.max_pages_per_seq * s.page_size;
+  p.block_n = ch.block_n;
+  p.scale_log2 = scale * kLog2eHost;
+  p.cap_log2 = s.soft_cap > 0.f ? s.soft_cap * kLog2eHost : 0.f;
+  p.scale_over_cap = s.soft_cap > 0.f ? scale / s.soft_cap : 0.f;
+  p.window = s.window;
+  p.sinks = sinks;
+  p.out = static_cast<uint16_t*>(out);
+  p.out_stride_tok = out_stride_tok;
+  p.out_stride_head = out_stride_head;
+  p.lse = lse;
+  uint8_t* sc = static_cast<uint8_t*>(scratch);
+  p.err = reinterpret_cast<uint32_t*>(sc);
+  p.work_count = reinterpret_cast<int*>(sc + 16);
+  p.work = reinterpret_cast<int2*>(sc + kScratchHeaderBytes);
+  p.work_cap = static_cast<int>((plan->scratch_bytes - kScratchHeaderBytes) / 8);
+  const int64_t cap_items = plan->grid[0] / s.num_kv_heads;
+  if (p.work_cap > cap_items) p.work_cap = static_cast<int>(cap_items);
+
+  cudaError_t e;
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  switch (s.head_dim) {
+    case 64: e = launch_ext<64, 128, 4>(tmq, tmk, tmv, p, strm); break;
+    case 128: e = launch_ext<128, 128, 2>(tmq, tmk, tmv, p, strm); break;
+    default: e = launch_ext<256, 64, 2>(tmq, tmk, tmv, p, strm); break;
+  }
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "pa.h"
+
 namespace pa {
 
 // Scratch header: the first 256 bytes of every scratch workspace.
@@ -52,6 +54,15 @@ struct DecodeConfig {
   int warps;
   int smem_bytes;
 };
+
+// Host helpers shared by the entry points (api.cu).
+pa_status validate_shape(const pa_shape& s);
+pa_status check_kv(const pa_shape& s, const void* k, const void* v, int64_t st_page, int64_t st_tok,
+                   int64_t st_head, int32_t num_pages);
+pa_status make_kv_map(CUtensorMap* map, const void* base, bool fp8, int D, int Hkv, int ps, int num_pages,
+                      int64_t st_page, int64_t st_tok, int64_t st_head, int box_rows);
+pa_status make_q_map(CUtensorMap* map, const void* base, int D, int Hq, int rows, int64_t st_tok, int64_t st_head,
+                     int group, int rows_per_box);
 
 // Kernel-variant table shared by the planner and the launcher.
 DecodeConfig decode_config(int head_dim, bool fp8, int group, int bt_cache);

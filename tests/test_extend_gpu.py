@@ -1,0 +1,111 @@
+"""Extend (prefix-prefill) parity: the tcgen05 path (through the C ABI) against the oracle."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+from paged_kv_gqa_12_gb300 import workloads as wl
+from tests import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_gqa_12_gb300 import binding
+    binding.load()
+
+
+def _ext(seed, *, Hq, Hkv, D, ps, ctx, ql, **kw):
+    ctx = np.asarray(ctx)
+    ql = np.asarray(ql)
+    return wl.build_problem("extend", num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=ps,
+                            seq_lens=ctx + ql, query_lens=ql, seed=seed, **kw)
+
+
+# ragged: empty context, context shorter than a tile, multi-tile context,
+# query counts off tile boundaries, a single-query request
+CTX = [0, 5, 300, 1000, 129, 0]
+QL = [37, 1, 200, 64, 513, 128]
+
+VARIANTS = [
+    # Hq, Hkv, D, ps
+    (32, 8, 128, 16),
+    (8, 2, 64, 16),
+    (16, 8, 256, 32),
+    (64, 8, 128, 64),     # group 8
+    (16, 1, 128, 16),     # group 16
+    (8, 8, 64, 32),       # group 1
+    (12, 4, 128, 16),     # group 3: 126 of 128 rows used
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,ps", VARIANTS)
+@pytest.mark.parametrize("opts", [{}, {"window": 100, "sinks": True}, {"soft_cap": 8.0}])
+def test_extend_variants(Hq, Hkv, D, ps, opts):
+    p = _ext(Hq * 5 + D + ps, Hq=Hq, Hkv=Hkv, D=D, ps=ps, ctx=CTX, ql=QL, **opts)
+    ref_o, ref_l = oracle.attention(p)
+    out, lse = gh.run(p)
+    gh.assert_parity(out, lse, ref_o, ref_l, what=f"extend {Hq},{Hkv},{D},{ps} {opts}")
+
+
+def test_extend_identity_probe_bitwise():
+    # window 1: every query sees only its own key, whose V row must come back
+    # exactly; every unattended slot of the pool is NaN.
+    for (Hq, Hkv, D, ps) in VARIANTS:
+        p = _ext(7 + D, Hq=Hq, Hkv=Hkv, D=D, ps=ps, ctx=CTX, ql=QL, window=1)
+        out, _ = gh.run(p)
+        ref_o, _ = oracle.attention(p)
+        assert np.array_equal(out.astype(np.float64), ref_o), (Hq, Hkv, D, ps)
+
+
+def test_extend_page_permutation_bitwise():
+    p = _ext(17, Hq=32, Hkv=8, D=128, ps=16, ctx=CTX, ql=QL, sinks=True)
+    o1, l1 = gh.run(p)
+    rng = np.random.default_rng(5)
+    perm = rng.permutation(p.num_pages)
+    k2 = np.empty_like(p.k_cache)
+    v2 = np.empty_like(p.v_cache)
+    k2[perm] = p.k_cache
+    v2[perm] = p.v_cache
+    bt = p.block_table.copy()
+    used = bt != wl.BT_SENTINEL
+    bt[used] = perm[bt[used]]
+    o2, l2 = gh.run(dataclasses.replace(p, k_cache=k2, v_cache=v2, block_table=bt))
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_extend_single_query_matches_decode():
+    ctx = np.array([0, 17, 999, 4000])
+    e = _ext(27, Hq=32, Hkv=8, D=128, ps=16, ctx=ctx, ql=[1, 1, 1, 1], window=700, sinks=True)
+    oe, le = gh.run(e)
+    d = dataclasses.replace(e, mode="decode", query_start_loc=None)
+    od, ld = gh.run(d)
+    ref_o, ref_l = oracle.attention(e)
+    gh.assert_parity(oe, le, ref_o, ref_l, what="extend q=1")
+    gh.assert_parity(od, ld, ref_o, ref_l, what="decode")
+
+
+def test_extend_empty_request_rows():
+    # zero new tokens for some requests: nothing to compute for them
+    p = _ext(37, Hq=8, Hkv=2, D=64, ps=16, ctx=[10, 50, 0, 7], ql=[0, 33, 5, 0])
+    ref_o, ref_l = oracle.attention(p)
+    out, lse = gh.run(p)
+    gh.assert_parity(out, lse, ref_o, ref_l)
+
+
+def test_extend_config4_full_sampled():
+    p = wl.config_problem(4)
+    out, lse = gh.run(p)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    rng = np.random.default_rng(4)
+    qsl = p.query_start_loc
+    rows = [int(qsl[b]) for b in range(p.batch)] + [int(qsl[b + 1]) - 1 for b in range(p.batch)]
+    rows += list(rng.choice(p.num_rows, size=48, replace=False))
+    rows = np.unique(np.array(rows, np.int32))
+    ref_o, ref_l = oracle.attention(p, rows=rows)
+    gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what="config 4")
