@@ -177,6 +177,24 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
   return true;
 }
 
+// 2^x on the FMA pipe, for part of the exponentials that would otherwise
+// queue behind the MUFU unit.  x = n + f with n the nearest integer (found by
+// adding and subtracting 1.5 * 2^23, whose float spacing is 1), 2^f from a
+// degree-3 polynomial fitted for minimum relative error on [-0.5, 0.5] (max
+// relative error 7.5e-5, well under the 2^-9 rounding P gets as bf16), and n
+// added to the exponent field.  x is clamped to >= -126 (the result is then
+// ~1e-38 instead of 0; used only where no score is masked).
+__device__ __forceinline__ float ex2_fma(float x) {
+  x = fmaxf(x, -126.0f);
+  const float r = __fadd_rn(x, 12582912.0f);
+  const float n = __fsub_rn(r, 12582912.0f);
+  const float f = __fsub_rn(x, n);
+  float q = fmaf(f, 0x1.c3f6a6p-5f, 0x1.f0ddccp-3f);
+  q = fmaf(q, f, 0x1.62f31ap-1f);
+  q = fmaf(q, f, 0x1.fff694p-1f);
+  return __int_as_float(__float_as_int(q) + (__float_as_int(r) << 23));
+}
+
 template <int D, int BN, int NST>
 struct ExtTraits {
   static constexpr int NCH = D / 64;                 // 128-byte column chunks per row
@@ -184,8 +202,7 @@ struct ExtTraits {
   static constexpr int Q_BYTES = NCH * Q_CHUNK;
   static constexpr int KV_CHUNK = BN * 128;
   static constexpr int TILE = NCH * KV_CHUNK;        // K (or V) tile
-  static constexpr int STAGE = 2 * TILE;
-  static constexpr int SMEM_DATA = Q_BYTES + NST * STAGE;
+  static constexpr int SMEM_DATA = Q_BYTES + 2 * NST * TILE;  // Q, K ring, V ring
   static constexpr int SMEM = 1024 + SMEM_DATA + 256;
   static constexpr uint32_t TMEM_O = 256;            // O columns start
   static_assert(2 * BN <= 256 && D <= 256, "TMEM plan: two S buffers in [0,256), O in [256,512)");
@@ -213,12 +230,15 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = smem;
-  uint8_t* kv_s = smem + T::Q_BYTES;
+  uint8_t* k_s = smem + T::Q_BYTES;
+  uint8_t* v_s = k_s + NST * T::TILE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::SMEM_DATA);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + NST;
-  uint64_t* s_full = kv_empty + NST;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + NST;
+  uint64_t* v_full = k_empty + NST;
+  uint64_t* v_empty = v_full + NST;
+  uint64_t* s_full = v_empty + NST;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 2);
@@ -234,8 +254,10 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     prefetch_tensormap(&tmv);
     mbar_init(q_full, 1);
     for (int i = 0; i < NST; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -249,11 +271,16 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
+  if (warp == 0 || warp == 2) {
+    // ---------------- TMA producers: warp 0 -> Q and the K ring, warp 2 -> the V ring ----------------
+    const bool is_k = warp == 0;
+    const CUtensorMap* map = is_k ? &tmk : &tmv;
+    uint64_t* full = is_k ? k_full : v_full;
+    uint64_t* empty = is_k ? k_empty : v_empty;
+    uint8_t* ring = is_k ? k_s : v_s;
     const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
     bool ok = true;
-    if (lane == 0) {
+    if (is_k && lane == 0) {
       mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(T::NCH * p.tm * G * 128));
 #pragma unroll
       for (int c = 0; c < T::NCH; ++c) tma_load_3d(q_s + c * T::Q_CHUNK, &tmq, c * 64, kvh * G, qs + t0, q_full);
@@ -261,9 +288,9 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     const int npg = BN / ps;
     for (int j = 0; j < n && ok; ++j) {
       const int stage = j % NST;
-      if (j >= NST) ok = __all_sync(0xffffffffu, wait_or_abort(&kv_empty[stage], ((j / NST) - 1) & 1, p.err));
+      if (j >= NST) ok = __all_sync(0xffffffffu, wait_or_abort(&empty[stage], ((j / NST) - 1) & 1, p.err));
       if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&kv_full[stage], static_cast<uint32_t>(T::STAGE));
+      if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(T::TILE));
       __syncwarp();
       if (lane < npg) {
         const int k0 = (kt0 + j) * BN;
@@ -271,14 +298,9 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         // pages with no attended key are fetched out of bounds: TMA writes zeros
         const bool outside = (pg * ps >= L) || ((pg + 1) * ps <= lo_min);
         const int coord = outside ? p.num_pages : bt_row[pg];
-        uint8_t* ks = kv_s + stage * T::STAGE;
-        uint8_t* vs = ks + T::TILE;
+        uint8_t* dst = ring + stage * T::TILE + lane * ps * 128;
 #pragma unroll
-        for (int c = 0; c < T::NCH; ++c) {
-          const int dst = c * T::KV_CHUNK + lane * ps * 128;
-          tma_load_4d(ks + dst, &tmk, c * 64, kvh, 0, coord, &kv_full[stage]);
-          tma_load_4d(vs + dst, &tmv, c * 64, kvh, 0, coord, &kv_full[stage]);
-        }
+        for (int c = 0; c < T::NCH; ++c) tma_load_4d(dst + c * T::KV_CHUNK, map, c * 64, kvh, 0, coord, &full[stage]);
       }
     }
   } else if (warp == 1) {
@@ -287,17 +309,18 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       constexpr uint32_t idesc_qk = idesc_bf16(kRows, BN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(kRows, D, false, true);
       const uint32_t q_u = smem_u32(q_s);
-      const uint32_t kv_u = smem_u32(kv_s);
+      const uint32_t k_ring = smem_u32(k_s);
+      const uint32_t v_ring = smem_u32(v_s);
       bool ok = wait_or_abort(q_full, 0, p.err);
       tc_fence_after();
       for (int j = 0; j <= n && ok; ++j) {
         if (j < n) {
           const int stage = j % NST;
-          ok = wait_or_abort(&kv_full[stage], (j / NST) & 1, p.err);
+          ok = wait_or_abort(&k_full[stage], (j / NST) & 1, p.err);
           if (!ok) break;
           tc_fence_after();
           const uint32_t tS = tbase + static_cast<uint32_t>((j & 1) * BN);
-          const uint32_t k_u = kv_u + stage * T::STAGE;
+          const uint32_t k_u = k_ring + stage * T::TILE;
 #pragma unroll
           for (int s = 0; s < D / 16; ++s) {
             const uint64_t ad = sdesc_sw128(q_u + (s >> 2) * T::Q_CHUNK + (s & 3) * 32, 16, 1024);
@@ -305,22 +328,24 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
             umma_ss(tS, ad, bd, idesc_qk, s > 0 ? 1u : 0u);
           }
           umma_commit(&s_full[j & 1]);
+          umma_commit(&k_empty[stage]);
         }
         if (j >= 1) {
           const int jj = j - 1;
           const int st = jj % NST;
-          ok = wait_or_abort(&p_full[jj & 1], (jj >> 1) & 1, p.err);
+          ok = wait_or_abort(&p_full[jj & 1], (jj >> 1) & 1, p.err) &&
+               wait_or_abort(&v_full[st], (jj / NST) & 1, p.err);
           if (!ok) break;
           tc_fence_after();
           const uint32_t tP = tbase + static_cast<uint32_t>((jj & 1) * BN);
-          const uint32_t v_u = kv_u + st * T::STAGE + T::TILE;
+          const uint32_t v_u = v_ring + st * T::TILE;
 #pragma unroll
           for (int s = 0; s < BN / 16; ++s) {
             const uint64_t bd = sdesc_sw128(v_u + s * 16 * 128, T::KV_CHUNK, 1024);
             umma_ts(tbase + T::TMEM_O, tP + s * 8, bd, idesc_pv, (jj > 0 || s > 0) ? 1u : 0u);
           }
           umma_commit(&o_done[jj & 1]);
-          umma_commit(&kv_empty[st]);
+          umma_commit(&v_empty[st]);
         }
       }
     }
@@ -335,6 +360,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     const int pos = ctx + min(tok, t_end - 1);
     const int lo = p.window > 0 ? pos - p.window + 1 : INT_MIN / 2;
     const bool capped = p.cap_log2 > 0.f;
+    const bool plain = !capped && p.scale_log2 > 0.f;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
@@ -348,30 +374,57 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       tmem_wait_ld();
       const bool full = (k0 >= lo) && (k0 + BN - 1 <= pos);
-      float mx = -INFINITY;
+      // unmasked tile for every row of the warp, plain scaling: the max is
+      // taken on raw scores and the scale folds into the exponent's FFMA
+      const bool fast = plain && __all_sync(0xffffffffu, full);
+      float mx8[8];
 #pragma unroll
-      for (int i = 0; i < BN; ++i) {
-        float v = __uint_as_float(sr[i]);
-        v = capped ? p.cap_log2 * tanhf(v * p.scale_over_cap) : v * p.scale_log2;
-        if (!full && (k0 + i > pos || k0 + i < lo)) v = -INFINITY;
-        sr[i] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+      for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
+      if (fast) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < BN; ++i) {
+          float v = __uint_as_float(sr[i]);
+          v = capped ? p.cap_log2 * tanhf(v * p.scale_over_cap) : v * p.scale_log2;
+          if (!full && (k0 + i > pos || k0 + i < lo)) v = -INFINITY;
+          sr[i] = __float_as_uint(v);
+          mx8[i & 7] = fmaxf(mx8[i & 7], v);
+        }
       }
+      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      if (fast) mx *= p.scale_log2;
       const float m_new = fmaxf(m_run, mx);
       const bool need = m_new > m_run + kRescaleThreshold;
       const bool any_need = __any_sync(0xffffffffu, need);
       const float m_use = need ? m_new : m_run;
       const float m_base = (m_use == -INFINITY) ? 0.f : m_use;
       const float alpha = (m_use == m_run || m_use == -INFINITY) ? 1.f : ex2(m_run - m_use);
-      float ls = 0.f;
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[BN / 2];
+      if (fast) {
+        // one exponential in four on the FMA pipe, the rest on MUFU
 #pragma unroll
-      for (int i = 0; i < BN / 2; ++i) {
-        const float p0 = ex2(__uint_as_float(sr[2 * i]) - m_base);
-        const float p1 = ex2(__uint_as_float(sr[2 * i + 1]) - m_base);
-        ls += p0 + p1;
-        pk[i] = pack_bf16x2(p0, p1);
+        for (int i = 0; i < BN / 2; ++i) {
+          const float x0 = fmaf(__uint_as_float(sr[2 * i]), p.scale_log2, -m_base);
+          const float x1 = fmaf(__uint_as_float(sr[2 * i + 1]), p.scale_log2, -m_base);
+          const float p0 = ex2(x0);
+          const float p1 = ((i & 1) == 1) ? ex2_fma(x1) : ex2(x1);
+          ls4[i & 3] += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < BN / 2; ++i) {
+          const float p0 = ex2(__uint_as_float(sr[2 * i]) - m_base);
+          const float p1 = ex2(__uint_as_float(sr[2 * i + 1]) - m_base);
+          ls4[i & 3] += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
       }
+      const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       l_run = l_run * alpha + ls;
       m_run = m_use;
 #pragma unroll
@@ -397,7 +450,10 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       // value rows past the sequence end inside the last page of this tile
       const int pend = min(k0 + BN, ((L + ps - 1) / ps) * ps);
       if (L < pend) {
-        uint8_t* vs = kv_s + (j % NST) * T::STAGE + T::TILE;
+        // V of this tile must have landed before its rows are overwritten
+        ok = __all_sync(0xffffffffu, wait_or_abort(&v_full[j % NST], (j / NST) & 1, p.err));
+        if (!ok) break;
+        uint8_t* vs = v_s + (j % NST) * T::TILE;
         const int nrows = pend - L;
         const int units = nrows * T::NCH * 8;   // 16-byte units
         for (int u = r; u < units; u += kRows) {
@@ -478,7 +534,7 @@ struct ExtChoice {
 
 ExtChoice ext_choice(int D) {
   if (D == 64) return {128, 4, ExtTraits<64, 128, 4>::SMEM};
-  if (D == 128) return {128, 2, ExtTraits<128, 128, 2>::SMEM};
+  if (D == 128) return {128, 3, ExtTraits<128, 128, 3>::SMEM};
   return {64, 2, ExtTraits<256, 64, 2>::SMEM};
 }
 
@@ -603,7 +659,7 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
   switch (s.head_dim) {
     case 64: e = launch_ext<64, 128, 4>(tmq, tmk, tmv, p, strm); break;
-    case 128: e = launch_ext<128, 128, 2>(tmq, tmk, tmv, p, strm); break;
+    case 128: e = launch_ext<128, 128, 3>(tmq, tmk, tmv, p, strm); break;
     default: e = launch_ext<256, 64, 2>(tmq, tmk, tmv, p, strm); break;
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
