@@ -13,10 +13,11 @@
 //   * Tile = 128 query rows x one kv head: the G q heads of each token are
 //     packed into the MMA M dimension (row = token * G + head), so one K/V
 //     tile feeds all heads that share it.
-//   * Warp roles in a 256-thread CTA: warp 0 issues TMA (Q once; per key tile
-//     one box per page for K and V, page ids from the block table), warp 1
-//     allocates TMEM and issues tcgen05.mma from one thread, warps 4-7 run
-//     the softmax with one TMEM lane (= one query row) per thread.
+//   * Warp roles in a 224-thread CTA: warps 0 and 2 issue TMA (Q once, then
+//     the K ring and the V ring: one box per page, page ids from the block
+//     table), warp 1 allocates TMEM and issues tcgen05.mma from one thread,
+//     warps 3-6 run the softmax with one TMEM lane (= one query row) per
+//     thread.  Two CTAs share an SM where TMEM and shared memory allow.
 //   * S = Q K^T (M=128, N=BN keys) lands in one of two TMEM buffers, so the
 //     next tile's QK overlaps this tile's softmax; P (bf16) is written back
 //     over S and consumed from TMEM by O += P V (V read MN-major from shared
@@ -40,11 +41,10 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 224;     // warps: 0 = Q/K TMA, 1 = MMA, 2 = V TMA, 3-6 = softmax
 constexpr int kRows = 128;           // MMA M: query rows per tile
 constexpr int kSchedThreads = 1024;
 constexpr int kBuckets = 256;        // work classes for the longest-first order
-constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
@@ -195,7 +195,7 @@ __device__ __forceinline__ float ex2_fma(float x) {
   return __int_as_float(__float_as_int(q) + (__float_as_int(r) << 23));
 }
 
-template <int D, int BN, int NST>
+template <int D, int BN, int NST, int CPS>
 struct ExtTraits {
   static constexpr int NCH = D / 64;                 // 128-byte column chunks per row
   static constexpr int Q_CHUNK = kRows * 128;        // 16 KB
@@ -204,16 +204,18 @@ struct ExtTraits {
   static constexpr int TILE = NCH * KV_CHUNK;        // K (or V) tile
   static constexpr int SMEM_DATA = Q_BYTES + 2 * NST * TILE;  // Q, K ring, V ring
   static constexpr int SMEM = 1024 + SMEM_DATA + 256;
-  static constexpr uint32_t TMEM_O = 256;            // O columns start
-  static_assert(2 * BN <= 256 && D <= 256, "TMEM plan: two S buffers in [0,256), O in [256,512)");
+  static constexpr uint32_t TMEM_COLS = 512 / CPS;   // CPS CTAs share an SM's 512 columns
+  static constexpr uint32_t TMEM_O = 2 * BN;         // two S buffers, then O
+  static_assert(2 * BN + D <= static_cast<int>(TMEM_COLS), "TMEM plan: S0, S1, O");
+  static_assert(CPS * SMEM <= 232448, "shared memory for CPS CTAs per SM");
   static_assert(BN % 64 == 0, "P is stored 32 columns (64 keys) at a time");
 };
 
-template <int D, int BN, int NST>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int BN, int NST, int CPS>
+__global__ void __launch_bounds__(kThreads, CPS)
 extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const ExtendParams p) {
-  using T = ExtTraits<D, BN, NST>;
+  using T = ExtTraits<D, BN, NST, CPS>;
   const int idx = blockIdx.x / p.num_kv_heads;
   const int kvh = blockIdx.x - idx * p.num_kv_heads;
   if (idx >= *p.work_count) return;
@@ -247,7 +249,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) tmem_alloc(tmem_slot, T::TMEM_COLS);
   if (tid == 0) {
     prefetch_tensormap(&tmq);
     prefetch_tensormap(&tmk);
@@ -349,9 +351,11 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         }
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 3) {
     // ---------------- softmax warpgroup: one query row per thread ----------------
-    const int wq = warp - 4;
+    // warps 3-6 cover the four TMEM lane quarters (a warp may only access
+    // lanes 32 * (warp % 4) .. + 31)
+    const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const int tok = t0 + r / G;
@@ -509,17 +513,17 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tbase, kTmemCols);
+  if (warp == 1) tmem_dealloc(tbase, T::TMEM_COLS);
 }
 
-template <int D, int BN, int NST>
+template <int D, int BN, int NST, int CPS>
 cudaError_t launch_ext(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                        const ExtendParams& p, cudaStream_t stream) {
-  using T = ExtTraits<D, BN, NST>;
+  using T = ExtTraits<D, BN, NST, CPS>;
   extend_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kern = extend_attn_kernel<D, BN, NST>;
+  auto kern = extend_attn_kernel<D, BN, NST, CPS>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
   if (e != cudaSuccess) return e;
   const int64_t blocks = static_cast<int64_t>(p.work_cap) * p.num_kv_heads;
@@ -532,10 +536,13 @@ struct ExtChoice {
   int block_n, stages, smem;
 };
 
+// Two CTAs per SM where TMEM and shared memory allow (64-key tiles, 256
+// TMEM columns each): one CTA's prologue, epilogue and softmax overlap the
+// other's MMAs.  head_dim 256 needs 256 O columns, so one CTA per SM.
 ExtChoice ext_choice(int D) {
-  if (D == 64) return {128, 4, ExtTraits<64, 128, 4>::SMEM};
-  if (D == 128) return {128, 3, ExtTraits<128, 128, 3>::SMEM};
-  return {64, 2, ExtTraits<256, 64, 2>::SMEM};
+  if (D == 64) return {64, 4, ExtTraits<64, 64, 4, 2>::SMEM};
+  if (D == 128) return {64, 2, ExtTraits<128, 64, 2, 2>::SMEM};
+  return {64, 2, ExtTraits<256, 64, 2, 1>::SMEM};
 }
 
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -658,9 +665,9 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
   cudaError_t e;
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
   switch (s.head_dim) {
-    case 64: e = launch_ext<64, 128, 4>(tmq, tmk, tmv, p, strm); break;
-    case 128: e = launch_ext<128, 128, 3>(tmq, tmk, tmv, p, strm); break;
-    default: e = launch_ext<256, 64, 2>(tmq, tmk, tmv, p, strm); break;
+    case 64: e = launch_ext<64, 64, 4, 2>(tmq, tmk, tmv, p, strm); break;
+    case 128: e = launch_ext<128, 64, 2, 2>(tmq, tmk, tmv, p, strm); break;
+    default: e = launch_ext<256, 64, 2, 1>(tmq, tmk, tmv, p, strm); break;
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
