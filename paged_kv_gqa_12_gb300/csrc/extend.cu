@@ -88,6 +88,17 @@ __device__ __forceinline__ bool item_range(const ExtendParams& p, int b, int mt,
   return true;
 }
 
+// Key tiles of query tile mt of a request (its cost): keys from the window
+// start of its first row to its last row's position.
+__device__ __forceinline__ int tile_cost(int ctx, int qlen, int mt, int tm, int window, int bn) {
+  const int t0 = mt * tm;
+  const int t_end = min(qlen, t0 + tm);
+  const int pos_min = ctx + t0;
+  const int pos_max = ctx + t_end - 1;
+  const int lo = window > 0 ? max(0, pos_min - window + 1) : 0;
+  return pos_max / bn - lo / bn + 1;
+}
+
 __global__ void __launch_bounds__(kSchedThreads) extend_schedule_kernel(const ExtendParams p) {
   __shared__ int s_hist[kBuckets];
   __shared__ int s_off[kBuckets];
@@ -101,18 +112,19 @@ __global__ void __launch_bounds__(kSchedThreads) extend_schedule_kernel(const Ex
   const int b1 = min(p.batch, b0 + per);
   int local = 0;
   for (int b = b0; b < b1; ++b) {
-    const int qlen = p.qsl[b + 1] - p.qsl[b];
-    if (qlen <= 0) continue;
+    const int qs = p.qsl[b];
+    const int qlen = p.qsl[b + 1] - qs;
+    const int L = p.seq_lens[b];
+    if (qlen == 0) continue;
+    if (qlen < 0 || L < qlen || L > p.max_kv || qs < 0 || qs + qlen > p.total_q) {
+      atomicOr(p.err, kErrCapacity);
+      continue;
+    }
     const int nmt = (qlen + p.tm - 1) / p.tm;
     for (int mt = 0; mt < nmt; ++mt) {
-      int qs, ql, ctx, t0, te, lo, kt0, n;
-      if (!item_range(p, b, mt, qs, ql, ctx, t0, te, lo, kt0, n)) {
-        atomicOr(p.err, kErrCapacity);
-        continue;
-      }
-      atomicAdd(&s_hist[min(n, kBuckets - 1)], 1);
-      ++local;
+      atomicAdd(&s_hist[min(tile_cost(L - qlen, qlen, mt, p.tm, p.window, p.block_n), kBuckets - 1)], 1);
     }
+    local += nmt;
   }
   atomicAdd(&s_total, local);
   __syncthreads();
@@ -141,13 +153,13 @@ __global__ void __launch_bounds__(kSchedThreads) extend_schedule_kernel(const Ex
   }
   __syncthreads();
   for (int b = b0; b < b1; ++b) {
-    const int qlen = p.qsl[b + 1] - p.qsl[b];
-    if (qlen <= 0) continue;
+    const int qs = p.qsl[b];
+    const int qlen = p.qsl[b + 1] - qs;
+    const int L = p.seq_lens[b];
+    if (qlen <= 0 || L < qlen || L > p.max_kv || qs < 0 || qs + qlen > p.total_q) continue;
     const int nmt = (qlen + p.tm - 1) / p.tm;
     for (int mt = 0; mt < nmt; ++mt) {
-      int qs, ql, ctx, t0, te, lo, kt0, n;
-      if (!item_range(p, b, mt, qs, ql, ctx, t0, te, lo, kt0, n)) continue;
-      const int pos = atomicAdd(&s_off[min(n, kBuckets - 1)], 1);
+      const int pos = atomicAdd(&s_off[min(tile_cost(L - qlen, qlen, mt, p.tm, p.window, p.block_n), kBuckets - 1)], 1);
       if (pos < p.work_cap) p.work[pos] = make_int2(b, mt);
     }
   }
@@ -193,6 +205,20 @@ __device__ __forceinline__ float ex2_fma(float x) {
   q = fmaf(q, f, 0x1.62f31ap-1f);
   q = fmaf(q, f, 0x1.fff694p-1f);
   return __int_as_float(__float_as_int(q) + (__float_as_int(r) << 23));
+}
+
+// The same 2^x for a pair, with Blackwell's packed fp32x2 FADD/FFMA.
+__device__ __forceinline__ float2 ex2_fma2(float2 x) {
+  x.x = fmaxf(x.x, -126.0f);
+  x.y = fmaxf(x.y, -126.0f);
+  const float2 r = __fadd2_rn(x, make_float2(12582912.0f, 12582912.0f));
+  const float2 n = __fadd2_rn(r, make_float2(-12582912.0f, -12582912.0f));
+  const float2 f = __ffma2_rn(n, make_float2(-1.0f, -1.0f), x);
+  float2 q = __ffma2_rn(f, make_float2(0x1.c3f6a6p-5f, 0x1.c3f6a6p-5f), make_float2(0x1.f0ddccp-3f, 0x1.f0ddccp-3f));
+  q = __ffma2_rn(q, f, make_float2(0x1.62f31ap-1f, 0x1.62f31ap-1f));
+  q = __ffma2_rn(q, f, make_float2(0x1.fff694p-1f, 0x1.fff694p-1f));
+  return make_float2(__int_as_float(__float_as_int(q.x) + (__float_as_int(r.x) << 23)),
+                     __int_as_float(__float_as_int(q.y) + (__float_as_int(r.y) << 23)));
 }
 
 template <int D, int BN, int NST, int CPS>
@@ -406,20 +432,31 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       const float m_use = need ? m_new : m_run;
       const float m_base = (m_use == -INFINITY) ? 0.f : m_use;
       const float alpha = (m_use == m_run || m_use == -INFINITY) ? 1.f : ex2(m_run - m_use);
-      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[BN / 2];
+      float ls;
       if (fast) {
-        // one exponential in four on the FMA pipe, the rest on MUFU
+        // packed fp32x2 arithmetic; one pair in four takes its exponentials
+        // on the FMA pipe, the rest on MUFU
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nm2 = make_float2(-m_base, -m_base);
+        float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int i = 0; i < BN / 2; ++i) {
-          const float x0 = fmaf(__uint_as_float(sr[2 * i]), p.scale_log2, -m_base);
-          const float x1 = fmaf(__uint_as_float(sr[2 * i + 1]), p.scale_log2, -m_base);
-          const float p0 = ex2(x0);
-          const float p1 = ((i & 1) == 1) ? ex2_fma(x1) : ex2(x1);
-          ls4[i & 3] += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), sc2, nm2);
+          float2 e;
+          if ((i & 3) == 3) {
+            e = ex2_fma2(x);
+          } else {
+            e.x = ex2(x.x);
+            e.y = ex2(x.y);
+          }
+          ls2[i & 1] = __fadd2_rn(ls2[i & 1], e);
+          pk[i] = pack_bf16x2(e.x, e.y);
         }
+        const float2 t = __fadd2_rn(ls2[0], ls2[1]);
+        ls = t.x + t.y;
       } else {
+        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < BN / 2; ++i) {
           const float p0 = ex2(__uint_as_float(sr[2 * i]) - m_base);
@@ -427,8 +464,8 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
           ls4[i & 3] += p0 + p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
+        ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       }
-      const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       l_run = l_run * alpha + ls;
       m_run = m_use;
 #pragma unroll
@@ -446,7 +483,12 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
           tmem_ld32(tO + c * 32, u);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 v = __fmul2_rn(make_float2(__uint_as_float(u[i]), __uint_as_float(u[i + 1])),
+                                        make_float2(alpha, alpha));
+            u[i] = __float_as_uint(v.x);
+            u[i + 1] = __float_as_uint(v.y);
+          }
           tmem_st32(tO + c * 32, u);
         }
         tmem_wait_st();
