@@ -189,38 +189,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
   return true;
 }
 
-// 2^x on the FMA pipe, for part of the exponentials that would otherwise
-// queue behind the MUFU unit.  x = n + f with n the nearest integer (found by
-// adding and subtracting 1.5 * 2^23, whose float spacing is 1), 2^f from a
-// degree-3 polynomial fitted for minimum relative error on [-0.5, 0.5] (max
-// relative error 7.5e-5, well under the 2^-9 rounding P gets as bf16), and n
-// added to the exponent field.  x is clamped to >= -126 (the result is then
-// ~1e-38 instead of 0; used only where no score is masked).
-__device__ __forceinline__ float ex2_fma(float x) {
-  x = fmaxf(x, -126.0f);
-  const float r = __fadd_rn(x, 12582912.0f);
-  const float n = __fsub_rn(r, 12582912.0f);
-  const float f = __fsub_rn(x, n);
-  float q = fmaf(f, 0x1.c3f6a6p-5f, 0x1.f0ddccp-3f);
-  q = fmaf(q, f, 0x1.62f31ap-1f);
-  q = fmaf(q, f, 0x1.fff694p-1f);
-  return __int_as_float(__float_as_int(q) + (__float_as_int(r) << 23));
-}
-
-// The same 2^x for a pair, with Blackwell's packed fp32x2 FADD/FFMA.
-__device__ __forceinline__ float2 ex2_fma2(float2 x) {
-  x.x = fmaxf(x.x, -126.0f);
-  x.y = fmaxf(x.y, -126.0f);
-  const float2 r = __fadd2_rn(x, make_float2(12582912.0f, 12582912.0f));
-  const float2 n = __fadd2_rn(r, make_float2(-12582912.0f, -12582912.0f));
-  const float2 f = __ffma2_rn(n, make_float2(-1.0f, -1.0f), x);
-  float2 q = __ffma2_rn(f, make_float2(0x1.c3f6a6p-5f, 0x1.c3f6a6p-5f), make_float2(0x1.f0ddccp-3f, 0x1.f0ddccp-3f));
-  q = __ffma2_rn(q, f, make_float2(0x1.62f31ap-1f, 0x1.62f31ap-1f));
-  q = __ffma2_rn(q, f, make_float2(0x1.fff694p-1f, 0x1.fff694p-1f));
-  return make_float2(__int_as_float(__float_as_int(q.x) + (__float_as_int(r.x) << 23)),
-                     __int_as_float(__float_as_int(q.y) + (__float_as_int(r.y) << 23)));
-}
-
 template <int D, int BN, int NST, int CPS>
 struct ExtTraits {
   static constexpr int NCH = D / 64;                 // 128-byte column chunks per row
@@ -435,21 +403,16 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       uint32_t pk[BN / 2];
       float ls;
       if (fast) {
-        // packed fp32x2 arithmetic; one pair in four takes its exponentials
-        // on the FMA pipe, the rest on MUFU
+        // packed fp32x2 FFMA / FADD around the MUFU exponentials (moving part
+        // of the exponentials to a polynomial on the FMA pipe was measured
+        // slower: this loop is issue-bound, not MUFU-bound)
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
         const float2 nm2 = make_float2(-m_base, -m_base);
         float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int i = 0; i < BN / 2; ++i) {
           const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), sc2, nm2);
-          float2 e;
-          if ((i & 3) == 3) {
-            e = ex2_fma2(x);
-          } else {
-            e.x = ex2(x.x);
-            e.y = ex2(x.y);
-          }
+          const float2 e = make_float2(ex2(x.x), ex2(x.y));
           ls2[i & 1] = __fadd2_rn(ls2[i & 1], e);
           pk[i] = pack_bf16x2(e.x, e.y);
         }
