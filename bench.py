@@ -329,7 +329,7 @@ def run_ours(args):
         ext_ach = eflops / ext_mean / 1e12
         kernels["extend"] = {"bound": "tensor", "achieved": round(ext_ach, 2), "peak": bf16, "unit": "TFLOP/s",
                              "frac": round(ext_ach / bf16, 4),
-                             "traffic": recorded_traffic("extend_kernel", ["extend.cu", "ptx.cuh", "pa_internal.h"]),
+                             "traffic": recorded_traffic("extend_attn_kernel", ["extend.cu", "ptx.cuh", "tcgen05.cuh", "pa_internal.h"]),
                              "timed": "pa_extend call (scheduler + attention kernel), CUDA events, mean over steps",
                              "algorithmic_flops_per_launch": eflops, "peak_source": f"{peak_src} bf16_tflops (burst)"}
     dominant = "decode"
