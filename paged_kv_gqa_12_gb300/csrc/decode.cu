@@ -405,6 +405,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     }
   }
 
+  // the merge kernel may start launching; it waits for this grid's partials
+  pdl_launch_dependents();
+
   // ---- merge the 4 warps' states in shared memory ----------------------------
   // Every TMA a warp issued was waited for inside its loop, so its stage
   // buffers are free; each warp writes its state into its own region.
@@ -480,6 +483,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
 // LSE merge: one warp per (request, q head); lane owns D/32 consecutive dims.
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p) {
+  pdl_wait_primary();  // split partials complete and visible
   const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (wid >= p.batch * p.num_q_heads) return;
@@ -541,8 +545,16 @@ cudaError_t launch_variant(const CUtensorMap& tmk, const CUtensorMap& tmv, const
   }
   const int warps = p.batch * p.num_q_heads;
   if (warps > 0) {
-    decode_merge_kernel<D><<<(warps + 3) / 4, 128, 0, stream>>>(p);
-    e = cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((warps + 3) / 4);
+    cfg.blockDim = dim3(128);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, p);
   }
   return e;
 }

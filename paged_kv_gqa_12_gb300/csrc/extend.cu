@@ -100,6 +100,9 @@ __device__ __forceinline__ int tile_cost(int ctx, int qlen, int mt, int tm, int 
 }
 
 __global__ void __launch_bounds__(kSchedThreads) extend_schedule_kernel(const ExtendParams p) {
+  // the attention kernel may start launching now; it waits for this grid's
+  // results (griddepcontrol.wait) before it reads the work list
+  pdl_launch_dependents();
   __shared__ int s_hist[kBuckets];
   __shared__ int s_off[kBuckets];
   __shared__ int s_total;
@@ -212,6 +215,12 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   using T = ExtTraits<D, BN, NST, CPS>;
   const int idx = blockIdx.x / p.num_kv_heads;
   const int kvh = blockIdx.x - idx * p.num_kv_heads;
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmq);
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+  pdl_wait_primary();  // the scheduler's work list is complete and visible
   if (idx >= *p.work_count) return;
   // another CTA already failed: leave (CTA-uniform, before any TMEM allocation)
   if (__syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<volatile uint32_t*>(p.err) != 0u)) return;
@@ -245,9 +254,6 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
 
   if (warp == 1) tmem_alloc(tmem_slot, T::TMEM_COLS);
   if (tid == 0) {
-    prefetch_tensormap(&tmq);
-    prefetch_tensormap(&tmk);
-    prefetch_tensormap(&tmv);
     mbar_init(q_full, 1);
     for (int i = 0; i < NST; ++i) {
       mbar_init(&k_full[i], 1);
@@ -380,7 +386,8 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
       if (fast) {
 #pragma unroll
-        for (int i = 0; i < BN; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
+        for (int i = 0; i < BN / 2; ++i)
+          mx8[i & 7] = fmax3(mx8[i & 7], __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
       } else {
 #pragma unroll
         for (int i = 0; i < BN; ++i) {
@@ -391,8 +398,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
           mx8[i & 7] = fmaxf(mx8[i & 7], v);
         }
       }
-      float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
       if (fast) mx *= p.scale_log2;
       const float m_new = fmaxf(m_run, mx);
       const bool need = m_new > m_run + kRescaleThreshold;
@@ -532,8 +538,17 @@ cudaError_t launch_ext(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUt
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
   if (e != cudaSuccess) return e;
   const int64_t blocks = static_cast<int64_t>(p.work_cap) * p.num_kv_heads;
-  kern<<<static_cast<unsigned>(blocks), kThreads, T::SMEM, stream>>>(tmq, tmk, tmv, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = T::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmq, tmk, tmv, p);
 }
 
 // Per head_dim: keys per tile and pipeline stages (shared memory <= 227 KB).
