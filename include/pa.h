@@ -66,7 +66,10 @@ typedef enum {
 } pa_status;
 
 typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
-typedef enum { PA_MODE_DECODE = 0, PA_MODE_EXTEND = 1 } pa_mode;
+/* VERIFY: extend where every request brings the same small number q_len of
+ * new tokens (1 + speculative tokens) over a long context; planned and run
+ * like decode (split-KV + merge), entered through pa_extend. */
+typedef enum { PA_MODE_DECODE = 0, PA_MODE_EXTEND = 1, PA_MODE_VERIFY = 2 } pa_mode;
 
 /* Static problem description (capacities, never live lengths, except for the
  * optional host seq_lens hint given to pa_plan). */
@@ -85,6 +88,7 @@ typedef struct {
   float soft_cap;             /* 0 = off; else s = cap * tanh(s / cap) */
   int32_t num_splits;         /* decode: 0 = planner's choice, >0 = max KV splits per request */
   int32_t num_sms;            /* SMs to plan for; 0 = query the current device */
+  int32_t q_len;              /* verify: new tokens per request (q_len * Hq/Hkv <= 16); else ignored */
 } pa_shape;
 
 /* Plan produced by pa_plan; plain data, may be copied.  Fields other than
@@ -178,8 +182,11 @@ pa_status pa_decode_static_scratch(const pa_plan_t* plan,
  *   out             device bf16 [total_q, Hq, D]; lse device fp32 [total_q, Hq] or NULL
  * A scheduler kernel builds the (request, kv head, query tile) work list in
  * the scratch workspace from the device metadata, longest first; the
- * attention kernel is persistent and takes items from that list.  total_q
- * must not exceed plan->shape.max_total_q.  Other arguments as for pa_decode. */
+ * attention kernel takes items from that list.  total_q must not exceed
+ * plan->shape.max_total_q.  With a PA_MODE_VERIFY plan every request must
+ * hold exactly plan->shape.q_len rows (query_start_loc[b] = b * q_len,
+ * total_q = batch * q_len); the call runs the split-KV kernels and a bad
+ * packing sets the device error word.  Other arguments as for pa_decode. */
 pa_status pa_extend(const pa_plan_t* plan,
                     const void* q, int64_t q_stride_tok, int64_t q_stride_head,
                     const void* k_cache, const void* v_cache,

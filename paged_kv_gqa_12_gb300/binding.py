@@ -23,6 +23,7 @@ PA_ERR_DEVICE = 5
 
 MODE_DECODE = 0
 MODE_EXTEND = 1
+MODE_VERIFY = 2
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
 
@@ -46,6 +47,7 @@ class PaShape(ctypes.Structure):
         ("soft_cap", ctypes.c_float),
         ("num_splits", ctypes.c_int32),
         ("num_sms", ctypes.c_int32),
+        ("q_len", ctypes.c_int32),
     ]
 
 
@@ -131,12 +133,13 @@ def _check(status: int, where: str):
 def plan(*, mode: int, num_q_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
          kv_dtype: int = KV_BF16, max_batch: int, max_pages_per_seq: int, max_total_q: int = 0,
          window: int = 0, has_sinks: bool = False, soft_cap: float = 0.0, num_splits: int = 0,
-         num_sms: int = 0, host_seq_lens=None) -> PaPlan:
+         num_sms: int = 0, q_len: int = 0, host_seq_lens=None) -> PaPlan:
     """pa_plan.  ``host_seq_lens``: optional host int32 sequence of lengths."""
     s = PaShape(mode=mode, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
                 page_size=page_size, kv_dtype=kv_dtype, max_batch=max_batch,
                 max_pages_per_seq=max_pages_per_seq, max_total_q=max_total_q, window=window,
-                has_sinks=1 if has_sinks else 0, soft_cap=soft_cap, num_splits=num_splits, num_sms=num_sms)
+                has_sinks=1 if has_sinks else 0, soft_cap=soft_cap, num_splits=num_splits, num_sms=num_sms,
+                q_len=q_len)
     p = PaPlan()
     lens_arr, n = None, 0
     if host_seq_lens is not None:

@@ -43,7 +43,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 }  // namespace
 
 pa_status validate_shape(const pa_shape& s) {
-  if (s.mode != PA_MODE_DECODE && s.mode != PA_MODE_EXTEND) return PA_ERR_INVALID_ARG;
+  if (s.mode != PA_MODE_DECODE && s.mode != PA_MODE_EXTEND && s.mode != PA_MODE_VERIFY) return PA_ERR_INVALID_ARG;
   if (s.num_q_heads <= 0 || s.num_kv_heads <= 0 || s.num_q_heads % s.num_kv_heads != 0) return PA_ERR_INVALID_ARG;
   if (s.max_batch < 0 || s.max_pages_per_seq < 0 || s.max_total_q < 0 || s.window < 0 || s.num_splits < 0 ||
       s.num_sms < 0)
@@ -55,21 +55,33 @@ pa_status validate_shape(const pa_shape& s) {
   if (s.page_size != 16 && s.page_size != 32 && s.page_size != 64) return PA_ERR_UNSUPPORTED;
   if (s.num_q_heads / s.num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(s.max_pages_per_seq) * s.page_size > (int64_t{1} << 30)) return PA_ERR_UNSUPPORTED;
+  if (s.mode == PA_MODE_VERIFY) {
+    if (s.q_len < 1) return PA_ERR_INVALID_ARG;
+    if (s.q_len * (s.num_q_heads / s.num_kv_heads) > 16) return PA_ERR_UNSUPPORTED;  // rows per kv head
+  }
   return PA_OK;
 }
 
+// Query tokens per request on the split-KV path.
+int split_kv_qlen(const pa_shape& s) { return s.mode == PA_MODE_VERIFY ? s.q_len : 1; }
+
 namespace {
 
-// Attended keys of one decode request: min(L, W) (W = 0: off).
-int64_t decode_keys(int64_t L, int window) { return window > 0 ? std::min<int64_t>(L, window) : L; }
+// Keys a split-KV request attends to (union over its q_len queries): the
+// window of the first query reaches W keys back, the last query adds q_len - 1.
+int64_t decode_keys(int64_t L, int window, int q_len) {
+  return window > 0 ? std::min<int64_t>(L, static_cast<int64_t>(window) + q_len - 1) : L;
+}
 
 pa_status plan_decode(const pa_shape& s, const int32_t* host_lens, int32_t batch, int num_sms, pa_plan_t* out) {
   const int G = s.num_q_heads / s.num_kv_heads;
+  const int qlen = split_kv_qlen(s);
+  const int rows = G * qlen;
   const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
-  DecodeConfig cfg = decode_config(s.head_dim, fp8, G, 0);
+  DecodeConfig cfg = decode_config(s.head_dim, fp8, rows, 0);
   const int TS = cfg.tile_tokens;
   const int64_t max_len = static_cast<int64_t>(s.max_pages_per_seq) * s.page_size;
-  const int64_t max_n = decode_keys(max_len, s.window);
+  const int64_t max_n = decode_keys(max_len, s.window, qlen);
   // +1: a window start that is not tile-aligned adds one partial tile
   const int64_t max_tiles = max_n > 0 ? cdiv64(max_n, TS) + 1 : 1;
   int64_t split_tiles = 0, tps_max, max_splits;
@@ -81,14 +93,14 @@ pa_status plan_decode(const pa_shape& s, const int32_t* host_lens, int32_t batch
     if (host_lens) {
       for (int b = 0; b < batch; ++b) {
         const int64_t L = host_lens[b];
-        const int64_t n = decode_keys(L, s.window);
+        const int64_t n = decode_keys(L, s.window, qlen);
         if (n > 0) units += cdiv64(L, TS) - (L - n) / TS;
       }
       units *= s.num_kv_heads;
     } else {
       units = static_cast<int64_t>(s.max_batch) * s.num_kv_heads * max_tiles;
     }
-    const int ctas_per_sm = (decode_config(s.head_dim, fp8, G, 64).smem_bytes * 2 <= kMaxSmemPerCta) ? 2 : 1;
+    const int ctas_per_sm = (decode_config(s.head_dim, fp8, rows, 64).smem_bytes * 2 <= kMaxSmemPerCta) ? 2 : 1;
     const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm * 4;
     split_tiles = std::max<int64_t>(8, cdiv64(units, std::max<int64_t>(target, 1)));
     split_tiles = std::min<int64_t>(split_tiles, max_tiles);
@@ -97,7 +109,7 @@ pa_status plan_decode(const pa_shape& s, const int32_t* host_lens, int32_t batch
   }
   const int64_t bt_cache = cdiv64(tps_max * TS, s.page_size) + 2;
   if (bt_cache > (1 << 15)) return PA_ERR_UNSUPPORTED;
-  cfg = decode_config(s.head_dim, fp8, G, static_cast<int>(bt_cache));
+  cfg = decode_config(s.head_dim, fp8, rows, static_cast<int>(bt_cache));
   if (cfg.smem_bytes > kMaxSmemPerCta) return PA_ERR_UNSUPPORTED;
 
   out->tile_tokens = TS;
@@ -110,8 +122,8 @@ pa_status plan_decode(const pa_shape& s, const int32_t* host_lens, int32_t batch
   out->grid[0] = static_cast<int32_t>(max_splits);
   out->grid[1] = s.num_kv_heads;
   out->grid[2] = s.max_batch;
-  const int64_t rows = static_cast<int64_t>(s.max_batch) * s.num_q_heads * max_splits;
-  out->scratch_bytes = kScratchHeaderBytes + align_up(rows * s.head_dim * 4, 256) + align_up(rows * 4, 256);
+  const int64_t prow = static_cast<int64_t>(s.max_batch) * qlen * s.num_q_heads * max_splits;
+  out->scratch_bytes = kScratchHeaderBytes + align_up(prow * s.head_dim * 4, 256) + align_up(prow * 4, 256);
   out->launches = 2;  // split kernel + merge kernel
   return PA_OK;
 }
@@ -193,7 +205,7 @@ using namespace pa;
 
 extern "C" {
 
-int32_t pa_version(void) { return 100; }
+int32_t pa_version(void) { return 101; }
 
 const char* pa_status_string(pa_status status) {
   switch (status) {
@@ -226,7 +238,7 @@ pa_status pa_plan(const pa_shape* shape, const int32_t* host_seq_lens, int32_t b
   std::memset(&p, 0, sizeof p);
   p.shape = *shape;
   p.shape.num_sms = num_sms;
-  if (shape->mode == PA_MODE_DECODE) {
+  if (shape->mode == PA_MODE_DECODE || shape->mode == PA_MODE_VERIFY) {
     st = plan_decode(*shape, host_seq_lens, batch, num_sms, &p);
   } else {
     st = plan_extend(*shape, num_sms, &p);
@@ -242,9 +254,26 @@ pa_status pa_decode(const pa_plan_t* plan, const void* q, int64_t q_stride_tok, 
                     const int32_t* seq_lens, int32_t batch, float scale, const float* sinks, float k_scale,
                     float v_scale, void* out, int64_t out_stride_tok, int64_t out_stride_head, float* lse,
                     void* scratch, int64_t scratch_bytes, void* stream) {
+  if (!plan || plan->shape.mode != PA_MODE_DECODE) return PA_ERR_INVALID_ARG;
+  return run_split_kv(plan, q, q_stride_tok, q_stride_head, k_cache, v_cache, kv_stride_page, kv_stride_tok,
+                      kv_stride_head, num_pages, block_table, bt_stride, seq_lens, nullptr, batch, scale, sinks,
+                      k_scale, v_scale, out, out_stride_tok, out_stride_head, lse, scratch, scratch_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace pa {
+
+pa_status run_split_kv(const pa_plan_t* plan, const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                       const void* k_cache, const void* v_cache, int64_t kv_stride_page, int64_t kv_stride_tok,
+                       int64_t kv_stride_head, int32_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                       const int32_t* seq_lens, const int32_t* qsl, int32_t batch, float scale, const float* sinks,
+                       float k_scale, float v_scale, void* out, int64_t out_stride_tok, int64_t out_stride_head,
+                       float* lse, void* scratch, int64_t scratch_bytes, void* stream) {
   if (!plan) return PA_ERR_INVALID_ARG;
   const pa_shape& s = plan->shape;
-  if (s.mode != PA_MODE_DECODE || validate_shape(s) != PA_OK) return PA_ERR_INVALID_ARG;
+  if ((s.mode != PA_MODE_DECODE && s.mode != PA_MODE_VERIFY) || validate_shape(s) != PA_OK) return PA_ERR_INVALID_ARG;
+  if (s.mode == PA_MODE_VERIFY && !qsl) return PA_ERR_INVALID_ARG;
   if (batch < 0 || batch > s.max_batch) return PA_ERR_INVALID_ARG;
   if (batch > 65535) return PA_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale)) return PA_ERR_INVALID_ARG;
@@ -262,7 +291,8 @@ pa_status pa_decode(const pa_plan_t* plan, const void* q, int64_t q_stride_tok, 
 
   const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
   const int G = s.num_q_heads / s.num_kv_heads;
-  const DecodeConfig cfg = decode_config(s.head_dim, fp8, G, plan->bt_cache);
+  const int qlen = split_kv_qlen(s);
+  const DecodeConfig cfg = decode_config(s.head_dim, fp8, G * qlen, plan->bt_cache);
   const int box_rows = std::min(s.page_size, plan->tile_tokens);
   CUtensorMap tmk, tmv;
   if ((st = make_kv_map(&tmk, k_cache, fp8, s.head_dim, s.num_kv_heads, s.page_size, num_pages, kv_stride_page,
@@ -296,7 +326,7 @@ pa_status pa_decode(const pa_plan_t* plan, const void* q, int64_t q_stride_tok, 
   p.out_stride_head = out_stride_head;
   p.lse = lse;
   uint8_t* sc = static_cast<uint8_t*>(scratch);
-  const int64_t rows = static_cast<int64_t>(s.max_batch) * s.num_q_heads * plan->max_splits;
+  const int64_t rows = static_cast<int64_t>(s.max_batch) * qlen * s.num_q_heads * plan->max_splits;
   p.o_part = reinterpret_cast<float*>(sc + kScratchHeaderBytes);
   p.lse_part = reinterpret_cast<float*>(sc + kScratchHeaderBytes + align_up(rows * s.head_dim * 4, 256));
   p.tile_tokens = plan->tile_tokens;
@@ -304,11 +334,17 @@ pa_status pa_decode(const pa_plan_t* plan, const void* q, int64_t q_stride_tok, 
   p.split_tiles = plan->split_tiles;
   p.fixed_splits = s.num_splits > 0 ? plan->max_splits : 0;
   p.bt_cache = plan->bt_cache;
+  p.q_len = qlen;
+  p.qsl = qsl;
   p.err = reinterpret_cast<uint32_t*>(sc);
   const dim3 grid(plan->max_splits, s.num_kv_heads, batch);
   const cudaError_t e = launch_decode(cfg, tmk, tmv, p, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
+
+}  // namespace pa
+
+extern "C" {
 
 pa_status pa_scratch_init(void* scratch, void* stream) {
   if (!scratch) return PA_ERR_INVALID_ARG;

@@ -14,10 +14,13 @@
 //     its lane 0 refills with TMA tensor loads straight out of the pages
 //     (page id from a block-table slice staged in shared memory).  No
 //     producer warp, no cross-warp barrier in the main loop.
-//   * The G q heads that share a kv head form the N dimension of warp-level
-//     bf16 MMAs: S^T = K Q^T (M = 16 keys, N = 8 heads) and
-//     O^T += V^T P^T (M = 16 dims, N = 8 heads), so a K/V element fetched
-//     once serves all G heads, and the 8-wide N keeps G = 8 free of padding.
+//   * The G q heads that share a kv head (times the query tokens per request:
+//     1 for decode, 1 + speculative tokens for verify) form the N dimension
+//     of warp-level bf16 MMAs: S^T = K Q^T (M = 16 keys, N = 8 rows) and
+//     O^T += V^T P^T (M = 16 dims, N = 8 rows), so a K/V element fetched
+//     once serves all rows, and the 8-wide N keeps 8 rows free of padding.
+//     Verify rows mask keys after their own position (causal) and outside
+//     their own window.
 //     P^T is formed in registers with movmatrix.
 //   * fp8-e4m3 K/V are dequantised in registers to bf16 exactly as the
 //     prefix-prefill page does: bf16(float(code) * scale).
@@ -51,8 +54,9 @@ struct SplitRange {
 __device__ __forceinline__ SplitRange split_range(const DecodeParams& p, int L) {
   SplitRange r;
   r.hi = L;
-  // sliding window: decode query at pos L-1 keeps key j iff (L-1) - j < W
-  r.lo = (p.window > 0) ? max(0, L - p.window) : 0;
+  // the first query of the request sits at L - q_len; with a window it keeps
+  // key j iff (L - q_len) - j < W, and later queries keep a subset of later keys
+  r.lo = (p.window > 0) ? max(0, (L - p.q_len) - p.window + 1) : 0;
   const int ts = p.tile_tokens;
   if (r.hi <= r.lo) {
     r.tile0 = 0;
@@ -110,6 +114,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     return;
   }
 
+  const int qrow0 = b * p.q_len;   // first query row of the request
+  if (p.qsl != nullptr && (p.qsl[b] != qrow0 || p.qsl[b + 1] != qrow0 + p.q_len)) {
+    if (threadIdx.x == 0 && split == 0) atomicOr(p.err, kErrCapacity);   // not equal-length packing
+    return;
+  }
   const int tile_begin = r.tile0 + split * r.tiles_per_split;
   const int tile_end = min(tile_begin + r.tiles_per_split, r.tile0 + r.n_tiles);
   const int n_tiles = tile_end - tile_begin;
@@ -119,6 +128,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
   const int pg0 = (tile_begin * TS) / ps;
   const int pg1 = (tok_hi + ps - 1) / ps;   // <= ceil(L / ps): never past the request's pages
   const int G = p.group;
+  const int R = p.q_len * G;          // query rows per kv head: (token, head) pairs
+  // tiles where every row sees every key need no per-element mask
+  const int pos_first = L - p.q_len;  // position of the first query
+  const int lo_last = p.window > 0 ? (L - 1) - p.window + 1 : 0;
+  const int full_lo = max(tok_lo, lo_last);
+  const int full_hi = min(tok_hi, pos_first + 1);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -172,15 +187,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     }
   };
 
-  // Q^T fragments (MMA B operand: k = head_dim slot, n = head).
+  // Q^T fragments (MMA B operand: k = head_dim slot, n = query row).
   uint32_t qf[T::KS][NH8][2];
   {
-    const uint16_t* qb = p.q + static_cast<int64_t>(b) * p.q_stride_tok;
 #pragma unroll
     for (int j = 0; j < NH8; ++j) {
-      const int hh = j * 8 + g;
-      const bool ok = hh < G;
-      const uint16_t* qh = qb + static_cast<int64_t>(kvh * G + (ok ? hh : 0)) * p.q_stride_head;
+      const int rr = j * 8 + g;   // row = token * G + head
+      const bool ok = rr < R;
+      const int tq = ok ? rr / G : 0;
+      const int hq = ok ? rr - tq * G : 0;
+      const uint16_t* qh = p.q + static_cast<int64_t>(qrow0 + tq) * p.q_stride_tok +
+                           static_cast<int64_t>(kvh * G + hq) * p.q_stride_head;
 #pragma unroll
       for (int ks = 0; ks < T::KS; ++ks) {
         int d0, d1;
@@ -205,10 +222,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[i][j][e] = 0.f;
   float m_run[NH8][2], l_run[NH8][2];
+  int rpos[NH8][2], rlo[NH8][2];   // this thread's two rows: last and first attended key
 #pragma unroll
   for (int j = 0; j < NH8; ++j) {
     m_run[j][0] = m_run[j][1] = -INFINITY;
     l_run[j][0] = l_run[j][1] = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int rr = j * 8 + 2 * c + h;
+      rpos[j][h] = pos_first + min(rr, R - 1) / G;
+      rlo[j][h] = p.window > 0 ? rpos[j][h] - p.window + 1 : 0;
+    }
   }
 
   if (lane == 0) {
@@ -231,7 +255,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     const uint32_t kst_u = smem_u32(kst);
     const uint32_t vst_u = smem_u32(vst);
     const int t0 = (tile_begin + k) * TS;
-    const bool partial = (t0 < tok_lo) || (t0 + TS > tok_hi);
+    const bool partial = (t0 < full_lo) || (t0 + TS > full_hi);
 
     // ---- S^T = K Q^T ------------------------------------------------------
     float s[T::MT][NH8][4];
@@ -288,7 +312,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
           v = capped ? p.cap_log2 * tanhf(v * p.scale_over_cap) : v * p.scale_log2;
           if (partial) {
             const int tok = t0 + mt * 16 + g + ((e >> 1) << 3);
-            if (tok < tok_lo || tok >= tok_hi) v = -INFINITY;
+            if (tok < tok_lo || tok >= tok_hi || tok > rpos[j][e & 1] || tok < rlo[j][e & 1]) v = -INFINITY;
           }
           s[mt][j][e] = v;
           mx[j][e & 1] = fmaxf(mx[j][e & 1], v);
@@ -334,11 +358,22 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     // ---- O^T += V^T P^T -----------------------------------------------------
 #pragma unroll
     for (int mt = 0; mt < T::MT; ++mt) {
-      uint32_t pb[NH8][2];
+      // P = P_hi + P_lo, both bf16: two MMAs make the weights exact to ~2^-17
+      // (one bf16 P can be 2^-9 off, which a row with few attended keys does
+      // not average out); the tensor pipe has room, the kernel is HBM-bound.
+      uint32_t pb[NH8][2], pl[NH8][2];
 #pragma unroll
       for (int j = 0; j < NH8; ++j) {
-        pb[j][0] = movmatrix_t(pack_bf16x2(s[mt][j][0], s[mt][j][1]));
-        pb[j][1] = movmatrix_t(pack_bf16x2(s[mt][j][2], s[mt][j][3]));
+        const uint32_t h0 = pack_bf16x2(s[mt][j][0], s[mt][j][1]);
+        const uint32_t h1 = pack_bf16x2(s[mt][j][2], s[mt][j][3]);
+        const uint32_t l0 = pack_bf16x2(s[mt][j][0] - __uint_as_float(h0 << 16),
+                                        s[mt][j][1] - __uint_as_float(h0 & 0xffff0000u));
+        const uint32_t l1 = pack_bf16x2(s[mt][j][2] - __uint_as_float(h1 << 16),
+                                        s[mt][j][3] - __uint_as_float(h1 & 0xffff0000u));
+        pb[j][0] = movmatrix_t(h0);
+        pb[j][1] = movmatrix_t(h1);
+        pl[j][0] = movmatrix_t(l0);
+        pl[j][1] = movmatrix_t(l1);
       }
       // Masked keys have P = 0, but their V rows may be stale or NaN: zero
       // them in the fragment so 0 * NaN never reaches the accumulator.
@@ -361,7 +396,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
           a[2] &= vm_hi;
           a[3] &= vm_hi;
 #pragma unroll
-          for (int j = 0; j < NH8; ++j) mma_bf16(o[i][j], a, pb[j][0], pb[j][1]);
+          for (int j = 0; j < NH8; ++j) {
+            mma_bf16(o[i][j], a, pb[j][0], pb[j][1]);
+            mma_bf16(o[i][j], a, pl[j][0], pl[j][1]);
+          }
         }
       } else {
         // thread g owns output dims [g*D/8, (g+1)*D/8): m-tile i row g -> dim
@@ -392,7 +430,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
           a[2] = dequant_e4m3x2(y, p.v_scale) & vm_hi;
           a[3] = dequant_e4m3x2(y >> 16, p.v_scale) & vm_hi;
 #pragma unroll
-          for (int j = 0; j < NH8; ++j) mma_bf16(o[i][j], a, pb[j][0], pb[j][1]);
+          for (int j = 0; j < NH8; ++j) {
+            mma_bf16(o[i][j], a, pb[j][0], pb[j][1]);
+            mma_bf16(o[i][j], a, pl[j][0], pl[j][1]);
+          }
         }
       }
     }
@@ -440,8 +481,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
   __syncthreads();
 
   const bool direct = (r.n_splits == 1);
-  for (int e = tid; e < G * D; e += kWarps * 32) {
-    const int h = e / D;
+  for (int e = tid; e < R * D; e += kWarps * 32) {
+    const int h = e / D;   // row within this kv head's rows
     const int d = e - h * D;
     float M = -INFINITY;
 #pragma unroll
@@ -458,7 +499,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
       num += wob[h * D + d] * f;
       den += wob[T::HW * D + T::HW + h] * f;
     }
-    const int hq = kvh * G + h;
+    const int tq = h / G;
+    const int hq = kvh * G + (h - tq * G);
+    const int64_t orow = qrow0 + tq;
     if (direct) {
       float M2 = M, zs = 0.f;
       if (p.sinks != nullptr) {
@@ -469,26 +512,27 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
       const float f = ex2(M - M2);
       const float Z = den * f + zs;
       const float ov = (Z > 0.f) ? num * f / Z : 0.f;
-      p.out[static_cast<int64_t>(b) * p.out_stride_tok + static_cast<int64_t>(hq) * p.out_stride_head + d] =
+      p.out[orow * p.out_stride_tok + static_cast<int64_t>(hq) * p.out_stride_head + d] =
           __bfloat16_as_ushort(__float2bfloat16_rn(ov));
-      if (d == 0 && p.lse != nullptr) p.lse[static_cast<int64_t>(b) * p.num_q_heads + hq] = (M2 + lg2(Z)) * kLn2;
+      if (d == 0 && p.lse != nullptr) p.lse[orow * p.num_q_heads + hq] = (M2 + lg2(Z)) * kLn2;
     } else {
-      const int64_t row = (static_cast<int64_t>(b) * p.num_q_heads + hq) * p.max_splits + split;
+      const int64_t row = (orow * p.num_q_heads + hq) * p.max_splits + split;
       p.o_part[row * D + d] = (den > 0.f) ? num / den : 0.f;
       if (d == 0) p.lse_part[row] = (M + lg2(den)) * kLn2;
     }
   }
 }
 
-// LSE merge: one warp per (request, q head); lane owns D/32 consecutive dims.
+// LSE merge: one warp per (query row, q head); lane owns D/32 consecutive dims.
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p) {
   pdl_wait_primary();  // split partials complete and visible
   const int wid = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (wid >= p.batch * p.num_q_heads) return;
-  const int b = wid / p.num_q_heads;
-  const int hq = wid - b * p.num_q_heads;
+  if (wid >= p.batch * p.q_len * p.num_q_heads) return;
+  const int row = wid / p.num_q_heads;
+  const int hq = wid - row * p.num_q_heads;
+  const int b = row / p.q_len;
   const SplitRange r = split_range(p, p.seq_lens[b]);
   if (r.n_splits == 1) return;  // written by the split kernel
   if (r.n_splits > p.max_splits) {  // seq_lens beyond the planned capacity
@@ -498,12 +542,12 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
   constexpr int V = D / 32;
   const bool has_sink = p.sinks != nullptr;
   const float sk = has_sink ? p.sinks[hq] * kLog2e : -INFINITY;
-  uint16_t* outp = p.out + static_cast<int64_t>(b) * p.out_stride_tok + static_cast<int64_t>(hq) * p.out_stride_head;
+  uint16_t* outp = p.out + static_cast<int64_t>(row) * p.out_stride_tok + static_cast<int64_t>(hq) * p.out_stride_head;
   float acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = 0.f;
   float M = sk;
-  const int64_t row0 = (static_cast<int64_t>(b) * p.num_q_heads + hq) * p.max_splits;
+  const int64_t row0 = (static_cast<int64_t>(row) * p.num_q_heads + hq) * p.max_splits;
   for (int s = lane; s < r.n_splits; s += 32) M = fmaxf(M, p.lse_part[row0 + s] * kLog2e);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -528,7 +572,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
     *reinterpret_cast<uint32_t*>(outp + lane * V + v) = pack_bf16x2(acc[v] * inv, acc[v + 1] * inv);
   }
   if (lane == 0 && p.lse != nullptr) {
-    p.lse[static_cast<int64_t>(b) * p.num_q_heads + hq] = (M == -INFINITY) ? -INFINITY : (M + lg2(Z)) * kLn2;
+    p.lse[static_cast<int64_t>(row) * p.num_q_heads + hq] = (M == -INFINITY) ? -INFINITY : (M + lg2(Z)) * kLn2;
   }
 }
 
@@ -543,7 +587,7 @@ cudaError_t launch_variant(const CUtensorMap& tmk, const CUtensorMap& tmv, const
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const int warps = p.batch * p.num_q_heads;
+  const int warps = p.batch * p.q_len * p.num_q_heads;
   if (warps > 0) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((warps + 3) / 4);
@@ -586,11 +630,11 @@ cudaError_t launch_d(const DecodeConfig& cfg, const CUtensorMap& tmk, const CUte
 
 }  // namespace
 
-DecodeConfig decode_config(int head_dim, bool fp8, int group, int bt_cache) {
+DecodeConfig decode_config(int head_dim, bool fp8, int rows, int bt_cache) {
   DecodeConfig c{};
   c.head_dim = head_dim;
   c.fp8 = fp8;
-  c.nh8 = group <= 8 ? 1 : 2;
+  c.nh8 = rows <= 8 ? 1 : 2;
   c.warps = kWarps;
 #define PA_TILE_CASE(DD, F8)                                    \
   if (head_dim == DD && fp8 == F8) {                            \

@@ -176,6 +176,23 @@ __global__ void __launch_bounds__(kSchedThreads) extend_schedule_kernel(const Ex
   }
 }
 
+// tanh(x) = 1 - 2 / (e^(2x) + 1), from the definition, with the hardware
+// exp2 and a fast reciprocal: absolute error ~1e-7 (so ~5e-6 on a logit
+// capped at 50), and few registers -- it is inlined once per score.
+__device__ __forceinline__ float tanh_exp2(float x) {
+  const float e = ex2(x * 2.8853900817779268f);  // e^(2x) = 2^(2x log2 e)
+  return 1.f - __fdividef(2.f, e + 1.f);
+}
+
+// A key tile in which some query row of the item masks some key (causal
+// diagonal, window edge or sequence end).  There the softmax weights are
+// passed as P = P_hi + P_lo (two bf16 halves, two PV MMAs): rows with only a
+// few attended keys live in such tiles, and one bf16 P (2^-9 relative) is not
+// averaged out over few keys.  Elsewhere every row attends to the whole tile.
+__device__ __forceinline__ bool split_p_tile(int k0, int bn, int pos_min, int lo_max, int L) {
+  return !(k0 >= lo_max && k0 + bn - 1 <= pos_min && k0 + bn <= L);
+}
+
 // Bounded wait that also gives up as soon as any CTA has reported an error,
 // so one failure cannot make every later CTA wait out its own timeout.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* err) {
@@ -208,6 +225,7 @@ struct ExtTraits {
   static_assert(BN % 64 == 0, "P is stored 32 columns (64 keys) at a time");
 };
 
+// Two CTAs per SM cap a thread at 128 registers (allocation counts 8 warps).
 template <int D, int BN, int NST, int CPS>
 __global__ void __launch_bounds__(kThreads, CPS)
 extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -313,6 +331,8 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       const uint32_t q_u = smem_u32(q_s);
       const uint32_t k_ring = smem_u32(k_s);
       const uint32_t v_ring = smem_u32(v_s);
+      const int pos_min = ctx + t0;
+      const int lo_max = p.window > 0 ? ctx + t_end - 1 - p.window + 1 : 0;
       bool ok = wait_or_abort(q_full, 0, p.err);
       tc_fence_after();
       for (int j = 0; j <= n && ok; ++j) {
@@ -341,10 +361,21 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
           tc_fence_after();
           const uint32_t tP = tbase + static_cast<uint32_t>((jj & 1) * BN);
           const uint32_t v_u = v_ring + st * T::TILE;
+          // P columns: k-step s (16 keys) at column 8s; on split tiles P_hi at
+          // 16s and P_lo at 16s + 8
+          const bool split = split_p_tile((kt0 + jj) * BN, BN, pos_min, lo_max, L);
+          const uint32_t pstep = split ? 16u : 8u;
 #pragma unroll
           for (int s = 0; s < BN / 16; ++s) {
             const uint64_t bd = sdesc_sw128(v_u + s * 16 * 128, T::KV_CHUNK, 1024);
-            umma_ts(tbase + T::TMEM_O, tP + s * 8, bd, idesc_pv, (jj > 0 || s > 0) ? 1u : 0u);
+            umma_ts(tbase + T::TMEM_O, tP + s * pstep, bd, idesc_pv, (jj > 0 || s > 0) ? 1u : 0u);
+          }
+          if (split) {
+#pragma unroll
+            for (int s = 0; s < BN / 16; ++s) {
+              const uint64_t bd = sdesc_sw128(v_u + s * 16 * 128, T::KV_CHUNK, 1024);
+              umma_ts(tbase + T::TMEM_O, tP + s * 16 + 8, bd, idesc_pv, 1u);
+            }
           }
           umma_commit(&o_done[jj & 1]);
           umma_commit(&v_empty[st]);
@@ -365,6 +396,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     const int lo = p.window > 0 ? pos - p.window + 1 : INT_MIN / 2;
     const bool capped = p.cap_log2 > 0.f;
     const bool plain = !capped && p.scale_log2 > 0.f;
+    const int lo_max_cta = p.window > 0 ? ctx + t_end - 1 - p.window + 1 : 0;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
@@ -378,67 +410,85 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       tmem_wait_ld();
       const bool full = (k0 >= lo) && (k0 + BN - 1 <= pos);
-      // unmasked tile for every row of the warp, plain scaling: the max is
-      // taken on raw scores and the scale folds into the exponent's FFMA
-      const bool fast = plain && __all_sync(0xffffffffu, full);
+      const bool split = split_p_tile(k0, BN, ctx + t0, lo_max_cta, L);
       float mx8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
-      if (fast) {
+      if (plain) {
+        // raw scores: masked keys become -inf (it stays -inf through the
+        // positive scale); the max is taken raw and the scale folds into the
+        // exponent's FFMA
+        if (!full) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i)
+            if (k0 + i > pos || k0 + i < lo) sr[i] = __float_as_uint(-INFINITY);
+        }
 #pragma unroll
         for (int i = 0; i < BN / 2; ++i)
           mx8[i & 7] = fmax3(mx8[i & 7], __uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
       } else {
+        // soft-cap (or a non-positive scale): transform every score first
 #pragma unroll
         for (int i = 0; i < BN; ++i) {
           float v = __uint_as_float(sr[i]);
-          v = capped ? p.cap_log2 * tanhf(v * p.scale_over_cap) : v * p.scale_log2;
+          v = capped ? p.cap_log2 * tanh_exp2(v * p.scale_over_cap) : v * p.scale_log2;
           if (!full && (k0 + i > pos || k0 + i < lo)) v = -INFINITY;
           sr[i] = __float_as_uint(v);
           mx8[i & 7] = fmaxf(mx8[i & 7], v);
         }
       }
       float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-      if (fast) mx *= p.scale_log2;
+      if (plain) mx *= p.scale_log2;
       const float m_new = fmaxf(m_run, mx);
       const bool need = m_new > m_run + kRescaleThreshold;
       const bool any_need = __any_sync(0xffffffffu, need);
       const float m_use = need ? m_new : m_run;
       const float m_base = (m_use == -INFINITY) ? 0.f : m_use;
       const float alpha = (m_use == m_run || m_use == -INFINITY) ? 1.f : ex2(m_run - m_use);
-      uint32_t pk[BN / 2];
-      float ls;
-      if (fast) {
-        // packed fp32x2 FFMA / FADD around the MUFU exponentials (moving part
-        // of the exponentials to a polynomial on the FMA pipe was measured
-        // slower: this loop is issue-bound, not MUFU-bound)
-        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-        const float2 nm2 = make_float2(-m_base, -m_base);
-        float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      // exponentials with packed fp32x2 FFMA / FADD (moving part of them to a
+      // polynomial on the FMA pipe was measured slower: issue-bound, not
+      // MUFU-bound).  P overwrites the score registers it consumes: P_hi of
+      // pair i in sr[i]; on split tiles each 16-key block b holds its 8 P_hi
+      // columns then its 8 P_lo columns in sr[16b .. 16b + 15].
+      const float am = plain ? p.scale_log2 : 1.f;
+      const float2 am2 = make_float2(am, am);
+      const float2 nm2 = make_float2(-m_base, -m_base);
+      float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      if (split) {
+#pragma unroll
+        for (int blk = 0; blk < BN / 16; ++blk) {
+          float2 e[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int k = blk * 16 + 2 * i;
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), am2, nm2);
+            e[i] = make_float2(ex2(x.x), ex2(x.y));
+            ls2[i & 1] = __fadd2_rn(ls2[i & 1], e[i]);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t hi = pack_bf16x2(e[i].x, e[i].y);
+            sr[blk * 16 + i] = hi;
+            sr[blk * 16 + 8 + i] =
+                pack_bf16x2(e[i].x - __uint_as_float(hi << 16), e[i].y - __uint_as_float(hi & 0xffff0000u));
+          }
+        }
+      } else {
 #pragma unroll
         for (int i = 0; i < BN / 2; ++i) {
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), sc2, nm2);
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), am2, nm2);
           const float2 e = make_float2(ex2(x.x), ex2(x.y));
           ls2[i & 1] = __fadd2_rn(ls2[i & 1], e);
-          pk[i] = pack_bf16x2(e.x, e.y);
+          sr[i] = pack_bf16x2(e.x, e.y);
         }
-        const float2 t = __fadd2_rn(ls2[0], ls2[1]);
-        ls = t.x + t.y;
-      } else {
-        float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < BN / 2; ++i) {
-          const float p0 = ex2(__uint_as_float(sr[2 * i]) - m_base);
-          const float p1 = ex2(__uint_as_float(sr[2 * i + 1]) - m_base);
-          ls4[i & 3] += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
       }
+      const float2 lt = __fadd2_rn(ls2[0], ls2[1]);
+      const float ls = lt.x + lt.y;
       l_run = l_run * alpha + ls;
       m_run = m_use;
-#pragma unroll
-      for (int c = 0; c < BN / 64; ++c) tmem_st32(tS + c * 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[c * 32]));
+      static_assert(BN == 64, "P stores below assume 32-column halves");
+      tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
+      if (split) tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));   // over S already read
       tmem_wait_st();
       if (any_need && j > 0) {
         // O must hold PV of tile j-1 before it is rescaled (and no PV may run meanwhile)
@@ -616,6 +666,16 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
   (void)v_scale;
   if (!plan) return PA_ERR_INVALID_ARG;
   const pa_shape& s = plan->shape;
+  if (s.mode == PA_MODE_VERIFY) {
+    // equal, small query counts per request: the split-KV kernels, one query
+    // row per (token, head)
+    if (batch < 0 || batch > s.max_batch || total_q != batch * s.q_len) return PA_ERR_INVALID_ARG;
+    if (!query_start_loc && batch > 0) return PA_ERR_INVALID_ARG;
+    return run_split_kv(plan, q, q_stride_tok, q_stride_head, k_cache, v_cache, kv_stride_page, kv_stride_tok,
+                        kv_stride_head, num_pages, block_table, bt_stride, seq_lens, query_start_loc, batch, scale,
+                        sinks, k_scale, v_scale, out, out_stride_tok, out_stride_head, lse, scratch, scratch_bytes,
+                        stream);
+  }
   if (s.mode != PA_MODE_EXTEND || validate_shape(s) != PA_OK) return PA_ERR_INVALID_ARG;
   if (s.kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
   if (batch < 0 || batch > s.max_batch || total_q < 0 || total_q > s.max_total_q) return PA_ERR_INVALID_ARG;

@@ -42,13 +42,15 @@ struct DecodeParams {
   int split_tiles;            // >0: tiles per split (planner mode)
   int fixed_splits;           // >0: split count per request (fixed mode)
   int bt_cache;               // block-table entries staged per CTA
+  int q_len;                  // query tokens per request: 1 (decode) or 1 + speculative (verify)
+  const int32_t* qsl;         // verify: query_start_loc, checked to be b * q_len; null for decode
   uint32_t* err;              // scratch header error word
 };
 
 struct DecodeConfig {
   int head_dim;
   bool fp8;
-  int nh8;                    // ceil(group / 8)
+  int nh8;                    // ceil(query rows per kv head / 8)
   int tile_tokens;
   int stages;
   int warps;
@@ -64,8 +66,17 @@ pa_status make_kv_map(CUtensorMap* map, const void* base, bool fp8, int D, int H
 pa_status make_q_map(CUtensorMap* map, const void* base, int D, int Hq, int rows, int64_t st_tok, int64_t st_head,
                      int group, int rows_per_box);
 
+// Split-KV path for decode (q_len = 1, qsl = null) and verify (equal q_len
+// per request, qsl checked on the device).
+pa_status run_split_kv(const pa_plan_t* plan, const void* q, int64_t q_stride_tok, int64_t q_stride_head,
+                       const void* k_cache, const void* v_cache, int64_t kv_stride_page, int64_t kv_stride_tok,
+                       int64_t kv_stride_head, int32_t num_pages, const int32_t* block_table, int64_t bt_stride,
+                       const int32_t* seq_lens, const int32_t* qsl, int32_t batch, float scale, const float* sinks,
+                       float k_scale, float v_scale, void* out, int64_t out_stride_tok, int64_t out_stride_head,
+                       float* lse, void* scratch, int64_t scratch_bytes, void* stream);
+
 // Kernel-variant table shared by the planner and the launcher.
-DecodeConfig decode_config(int head_dim, bool fp8, int group, int bt_cache);
+DecodeConfig decode_config(int head_dim, bool fp8, int rows, int bt_cache);
 
 cudaError_t launch_decode(const DecodeConfig& cfg, const CUtensorMap& tmk, const CUtensorMap& tmv,
                           const DecodeParams& p, dim3 grid, cudaStream_t stream);

@@ -36,21 +36,26 @@ def upload(p, device="cuda"):
     return d
 
 
-def make_plan(p, num_splits=0, host_lens=True, max_batch=None):
+def make_plan(p, num_splits=0, host_lens=True, max_batch=None, verify=False):
     kv = pb.KV_FP8_E4M3 if p.kv_dtype == "fp8_e4m3" else pb.KV_BF16
     mode = pb.MODE_DECODE if p.mode == "decode" else pb.MODE_EXTEND
+    q_len = 0
+    if verify:
+        ql = p.query_lens()
+        assert p.mode == "extend" and np.all(ql == ql[0]), "verify needs equal query counts"
+        mode, q_len = pb.MODE_VERIFY, int(ql[0])
     return pb.plan(mode=mode, num_q_heads=p.num_q_heads, num_kv_heads=p.num_kv_heads,
                    head_dim=p.head_dim, page_size=p.page_size, kv_dtype=kv,
                    max_batch=max_batch or max(p.batch, 1), max_pages_per_seq=p.block_table.shape[1],
                    max_total_q=max(p.num_rows, 1), window=p.window, has_sinks=p.sinks is not None,
-                   soft_cap=p.soft_cap, num_splits=num_splits,
-                   host_seq_lens=p.seq_lens if (host_lens and p.mode == "decode") else None)
+                   soft_cap=p.soft_cap, num_splits=num_splits, q_len=q_len,
+                   host_seq_lens=p.seq_lens if (host_lens and (p.mode == "decode" or verify)) else None)
 
 
-def run(p, d=None, plan=None, num_splits=0, host_lens=True, with_lse=True):
+def run(p, d=None, plan=None, num_splits=0, host_lens=True, with_lse=True, verify=False):
     """Run decode or extend on the GPU; returns (out float32 [T,Hq,D], lse [T,Hq]) on the host."""
     d = d or upload(p)
-    plan = plan or make_plan(p, num_splits=num_splits, host_lens=host_lens)
+    plan = plan or make_plan(p, num_splits=num_splits, host_lens=host_lens, verify=verify)
     T, Hq, D = p.q.shape
     out = torch.full((T, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((T, Hq), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
