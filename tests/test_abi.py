@@ -183,3 +183,18 @@ def test_binding_fails_loudly_without_library(tmp_path):
             b2.load(str(tmp_path / "missing.so"))
     finally:
         importlib.reload(pb)
+
+
+@pytest.mark.parametrize("q_len,status", [(0, pb.PA_ERR_INVALID_ARG), (5, pb.PA_ERR_UNSUPPORTED)])
+def test_plan_verify_rejects(lib, q_len, status):
+    # 32 q heads over 8 kv heads: group 4, so at most 4 tokens per request
+    with pytest.raises(pb.PaError) as ei:
+        _plan(mode=pb.MODE_VERIFY, q_len=q_len, max_total_q=256)
+    assert ei.value.status == status
+
+
+def test_plan_verify_scratch_scales_with_q_len(lib):
+    one = _plan(mode=pb.MODE_VERIFY, q_len=1, max_total_q=64, num_splits=4)
+    four = _plan(mode=pb.MODE_VERIFY, q_len=4, max_total_q=256, num_splits=4)
+    assert four.scratch_bytes > 3 * (one.scratch_bytes - 256)
+    assert four.launches == 2
