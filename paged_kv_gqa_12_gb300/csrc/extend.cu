@@ -32,6 +32,7 @@
 //   * A one-CTA scheduler kernel builds the (request, query tile) list from
 //     the device metadata, heaviest first; CTA i takes item i / Hkv.
 #include <climits>
+#include <cmath>
 #include <cstdint>
 
 #include "extend.h"
@@ -61,6 +62,7 @@ struct ExtendParams {
   float scale_log2, cap_log2, scale_over_cap;
   int window;
   const float* sinks;
+  float k_scale, v_scale;   // fp8 cache: per-tensor dequantisation scales
   uint16_t* out;
   int64_t out_stride_tok, out_stride_head;
   float* lse;
@@ -209,7 +211,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
   return true;
 }
 
-template <int D, int BN, int NST, int CPS>
+template <int D, int BN, int NST, int CPS, bool FP8 = false>
 struct ExtTraits {
   static constexpr int NCH = D / 64;                 // 128-byte column chunks per row
   static constexpr int Q_CHUNK = kRows * 128;        // 16 KB
@@ -218,6 +220,12 @@ struct ExtTraits {
   static constexpr int TILE = NCH * KV_CHUNK;        // K (or V) tile
   static constexpr int SMEM_DATA = Q_BYTES + 2 * NST * TILE;  // Q, K ring, V ring
   static constexpr int SMEM = 1024 + SMEM_DATA + 256;
+  // fp8 cache: the e4m3 tile lands in the second half of the bf16 stage
+  // buffer, rows of RB8 bytes (row r under bf16 row r's upper chunks when
+  // D >= 128), and is dequantised in place
+  static constexpr int RB8 = D < 128 ? D : 128;      // bytes per fp8 box row
+  static constexpr int NCC8 = D / RB8;               // fp8 boxes per page
+  static constexpr int F8_OFF = TILE / 2;
   static constexpr uint32_t TMEM_COLS = 512 / CPS;   // CPS CTAs share an SM's 512 columns
   static constexpr uint32_t TMEM_O = 2 * BN;         // two S buffers, then O
   static_assert(2 * BN + D <= static_cast<int>(TMEM_COLS), "TMEM plan: S0, S1, O");
@@ -225,12 +233,67 @@ struct ExtTraits {
   static_assert(BN % 64 == 0, "P is stored 32 columns (64 keys) at a time");
 };
 
-// Two CTAs per SM cap a thread at 128 registers (allocation counts 8 warps).
+// In-place dequantisation of one e4m3 K or V tile (BN rows) into the bf16
+// layout the MMA reads (rows of 64-element chunks, 128-byte swizzle), by one
+// warp: element = bf16(float(code) * scale), as the prefix-prefill page does.
 template <int D, int BN, int NST, int CPS>
+__device__ __forceinline__ void dequant_tile(uint8_t* tile, float scale, int lane) {
+  using T = ExtTraits<D, BN, NST, CPS, true>;
+  constexpr int UPR = T::RB8 / 16;         // 16-byte fp8 units per box row
+  constexpr int U = T::NCC8 * UPR;         // units per key row
+  const uint8_t* f8 = tile + T::F8_OFF;
+  auto out_unit = [&](int r, int d16, const uint4& w) {
+    // 16 codes = dims [16 d16, 16 d16 + 16) -> two 16-byte bf16 units
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      o[2 * k] = dequant_e4m3x2(wv[k] & 0xffffu, scale);
+      o[2 * k + 1] = dequant_e4m3x2(wv[k] >> 16, scale);
+    }
+    const int chunk = d16 >> 2;
+    const int unit0 = (d16 & 3) * 2;
+    uint8_t* rowp = tile + chunk * T::KV_CHUNK + r * 128;
+    *reinterpret_cast<uint4*>(rowp + (((unit0) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(rowp + (((unit0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+  };
+  auto in_unit = [&](int r, int u) -> uint4 {
+    const int box = u / UPR, uu = u % UPR;
+    const int sw = T::RB8 == 128 ? (r & 7) : ((r >> 1) & 3);
+    return *reinterpret_cast<const uint4*>(f8 + box * BN * T::RB8 + r * T::RB8 + ((uu ^ sw) << 4));
+  };
+  if constexpr (D >= 128) {
+    // row r's e4m3 bytes lie under its own upper bf16 chunks: read the row, then write it
+#pragma unroll
+    for (int r = lane; r < BN; r += 32) {
+      uint4 w[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) w[u] = in_unit(r, u);
+#pragma unroll
+      for (int u = 0; u < U; ++u) out_unit(r, u, w[u]);
+    }
+  } else {
+    // 64-byte e4m3 rows straddle other rows' bf16 rows: read the whole tile first
+    constexpr int RPT = BN / 32;
+    uint4 w[RPT][U];
+#pragma unroll
+    for (int k = 0; k < RPT; ++k)
+#pragma unroll
+      for (int u = 0; u < U; ++u) w[k][u] = in_unit(lane + 32 * k, u);
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < RPT; ++k)
+#pragma unroll
+      for (int u = 0; u < U; ++u) out_unit(lane + 32 * k, u, w[k][u]);
+  }
+}
+
+// Two CTAs per SM cap a thread at 128 registers (allocation counts 8 warps).
+template <int D, int BN, int NST, int CPS, bool FP8>
 __global__ void __launch_bounds__(kThreads, CPS)
 extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                    const __grid_constant__ CUtensorMap tmv, const ExtendParams p) {
-  using T = ExtTraits<D, BN, NST, CPS>;
+  using T = ExtTraits<D, BN, NST, CPS, FP8>;
   const int idx = blockIdx.x / p.num_kv_heads;
   const int kvh = blockIdx.x - idx * p.num_kv_heads;
   if (threadIdx.x == 0) {
@@ -261,7 +324,9 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   uint64_t* k_empty = k_full + NST;
   uint64_t* v_full = k_empty + NST;
   uint64_t* v_empty = v_full + NST;
-  uint64_t* s_full = v_empty + NST;
+  uint64_t* k_land = v_empty + NST;   // fp8: the e4m3 tile has landed (before dequantisation)
+  uint64_t* v_land = k_land + NST;
+  uint64_t* s_full = v_land + NST;
   uint64_t* p_full = s_full + 2;
   uint64_t* o_done = p_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 2);
@@ -278,6 +343,8 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
+      mbar_init(&k_land[i], 1);
+      mbar_init(&v_land[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -306,21 +373,59 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       for (int c = 0; c < T::NCH; ++c) tma_load_3d(q_s + c * T::Q_CHUNK, &tmq, c * 64, kvh * G, qs + t0, q_full);
     }
     const int npg = BN / ps;
-    for (int j = 0; j < n && ok; ++j) {
-      const int stage = j % NST;
-      if (j >= NST) ok = __all_sync(0xffffffffu, wait_or_abort(&empty[stage], ((j / NST) - 1) & 1, p.err));
-      if (!ok) break;
-      if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(T::TILE));
-      __syncwarp();
-      if (lane < npg) {
-        const int k0 = (kt0 + j) * BN;
-        const int pg = k0 / ps + lane;
-        // pages with no attended key are fetched out of bounds: TMA writes zeros
-        const bool outside = (pg * ps >= L) || ((pg + 1) * ps <= lo_min);
-        const int coord = outside ? p.num_pages : bt_row[pg];
-        uint8_t* dst = ring + stage * T::TILE + lane * ps * 128;
+    // page coordinate of this lane's page of key tile j; pages with no
+    // attended key are fetched out of bounds, where TMA writes zeros
+    auto page_coord = [&](int j) {
+      const int pg = ((kt0 + j) * BN) / ps + lane;
+      const bool outside = (pg * ps >= L) || ((pg + 1) * ps <= lo_min);
+      return outside ? p.num_pages : bt_row[pg];
+    };
+    if constexpr (!FP8) {
+      for (int j = 0; j < n && ok; ++j) {
+        const int stage = j % NST;
+        if (j >= NST) ok = __all_sync(0xffffffffu, wait_or_abort(&empty[stage], ((j / NST) - 1) & 1, p.err));
+        if (!ok) break;
+        if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(T::TILE));
+        __syncwarp();
+        if (lane < npg) {
+          const int coord = page_coord(j);
+          uint8_t* dst = ring + stage * T::TILE + lane * ps * 128;
 #pragma unroll
-        for (int c = 0; c < T::NCH; ++c) tma_load_4d(dst + c * T::KV_CHUNK, map, c * 64, kvh, 0, coord, &full[stage]);
+          for (int c = 0; c < T::NCH; ++c) tma_load_4d(dst + c * T::KV_CHUNK, map, c * 64, kvh, 0, coord, &full[stage]);
+        }
+      }
+    } else {
+      // e4m3 tiles land in the stage (NST ahead), then this warp dequantises
+      // them in place and marks the stage full
+      uint64_t* land = is_k ? k_land : v_land;
+      const float scale = is_k ? p.k_scale : p.v_scale;
+      auto fetch = [&](int j) {
+        const int stage = j % NST;
+        if (lane == 0) mbar_arrive_expect_tx(&land[stage], static_cast<uint32_t>(BN * D));
+        __syncwarp();
+        if (lane < npg) {
+          const int coord = page_coord(j);
+          uint8_t* dst = ring + stage * T::TILE + T::F8_OFF + lane * ps * T::RB8;
+#pragma unroll
+          for (int c = 0; c < T::NCC8; ++c)
+            tma_load_4d(dst + c * BN * T::RB8, map, c * T::RB8, kvh, 0, coord, &land[stage]);
+        }
+      };
+      for (int j = 0; j < n && j < NST; ++j) fetch(j);
+      for (int j = 0; j < n && ok; ++j) {
+        const int stage = j % NST;
+        ok = __all_sync(0xffffffffu, wait_or_abort(&land[stage], (j / NST) & 1, p.err));
+        if (!ok) break;
+        dequant_tile<D, BN, NST, CPS>(ring + stage * T::TILE, scale, lane);
+        fence_proxy_async_smem();   // generic writes -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[stage]);
+        const int jn = j + NST;
+        if (jn < n) {
+          ok = __all_sync(0xffffffffu, wait_or_abort(&empty[stage], ((jn / NST) - 1) & 1, p.err));
+          if (!ok) break;
+          fetch(jn);
+        }
       }
     }
   } else if (warp == 1) {
@@ -577,14 +682,14 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   if (warp == 1) tmem_dealloc(tbase, T::TMEM_COLS);
 }
 
-template <int D, int BN, int NST, int CPS>
+template <int D, int BN, int NST, int CPS, bool FP8>
 cudaError_t launch_ext(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUtensorMap& tmv,
                        const ExtendParams& p, cudaStream_t stream) {
-  using T = ExtTraits<D, BN, NST, CPS>;
+  using T = ExtTraits<D, BN, NST, CPS, FP8>;
   extend_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kern = extend_attn_kernel<D, BN, NST, CPS>;
+  auto kern = extend_attn_kernel<D, BN, NST, CPS, FP8>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
   if (e != cudaSuccess) return e;
   const int64_t blocks = static_cast<int64_t>(p.work_cap) * p.num_kv_heads;
@@ -621,7 +726,6 @@ int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 pa_status plan_extend(const pa_shape& s, int num_sms, pa_plan_t* out) {
   (void)num_sms;
-  if (s.kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
   const int G = s.num_q_heads / s.num_kv_heads;
   const int tm = kRows / G;
   const ExtChoice ch = ext_choice(s.head_dim);
@@ -662,8 +766,6 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
                                const float* sinks, float k_scale, float v_scale, void* out, int64_t out_stride_tok,
                                int64_t out_stride_head, float* lse, void* scratch, int64_t scratch_bytes,
                                void* stream) {
-  (void)k_scale;
-  (void)v_scale;
   if (!plan) return PA_ERR_INVALID_ARG;
   const pa_shape& s = plan->shape;
   if (s.mode == PA_MODE_VERIFY) {
@@ -677,7 +779,8 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
                         stream);
   }
   if (s.mode != PA_MODE_EXTEND || validate_shape(s) != PA_OK) return PA_ERR_INVALID_ARG;
-  if (s.kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
+  const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
+  if (!std::isfinite(k_scale) || !std::isfinite(v_scale)) return PA_ERR_INVALID_ARG;
   if (batch < 0 || batch > s.max_batch || total_q < 0 || total_q > s.max_total_q) return PA_ERR_INVALID_ARG;
   if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PA_ERR_INVALID_ARG;
   if ((sinks != nullptr) != (s.has_sinks != 0)) return PA_ERR_INVALID_ARG;
@@ -703,10 +806,10 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
   if ((st = make_q_map(&tmq, q, s.head_dim, s.num_q_heads, total_q, q_stride_tok, q_stride_head, G, tm)) !=
       PA_OK)
     return st;
-  if ((st = make_kv_map(&tmk, k_cache, false, s.head_dim, s.num_kv_heads, s.page_size, num_pages,
+  if ((st = make_kv_map(&tmk, k_cache, fp8, s.head_dim, s.num_kv_heads, s.page_size, num_pages,
                                kv_stride_page, kv_stride_tok, kv_stride_head, s.page_size)) != PA_OK)
     return st;
-  if ((st = make_kv_map(&tmv, v_cache, false, s.head_dim, s.num_kv_heads, s.page_size, num_pages,
+  if ((st = make_kv_map(&tmv, v_cache, fp8, s.head_dim, s.num_kv_heads, s.page_size, num_pages,
                                kv_stride_page, kv_stride_tok, kv_stride_head, s.page_size)) != PA_OK)
     return st;
 
@@ -730,6 +833,8 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
   p.scale_over_cap = s.soft_cap > 0.f ? scale / s.soft_cap : 0.f;
   p.window = s.window;
   p.sinks = sinks;
+  p.k_scale = fp8 ? k_scale : 1.f;
+  p.v_scale = fp8 ? v_scale : 1.f;
   p.out = static_cast<uint16_t*>(out);
   p.out_stride_tok = out_stride_tok;
   p.out_stride_head = out_stride_head;
@@ -744,10 +849,13 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
 
   cudaError_t e;
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
-  switch (s.head_dim) {
-    case 64: e = launch_ext<64, 64, 4, 2>(tmq, tmk, tmv, p, strm); break;
-    case 128: e = launch_ext<128, 64, 2, 2>(tmq, tmk, tmv, p, strm); break;
-    default: e = launch_ext<256, 64, 2, 1>(tmq, tmk, tmv, p, strm); break;
+  switch (s.head_dim * 2 + (fp8 ? 1 : 0)) {
+    case 128: e = launch_ext<64, 64, 4, 2, false>(tmq, tmk, tmv, p, strm); break;
+    case 129: e = launch_ext<64, 64, 4, 2, true>(tmq, tmk, tmv, p, strm); break;
+    case 256: e = launch_ext<128, 64, 2, 2, false>(tmq, tmk, tmv, p, strm); break;
+    case 257: e = launch_ext<128, 64, 2, 2, true>(tmq, tmk, tmv, p, strm); break;
+    case 512: e = launch_ext<256, 64, 2, 1, false>(tmq, tmk, tmv, p, strm); break;
+    default: e = launch_ext<256, 64, 2, 1, true>(tmq, tmk, tmv, p, strm); break;
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

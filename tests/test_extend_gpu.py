@@ -109,3 +109,26 @@ def test_extend_config4_full_sampled():
     rows = np.unique(np.array(rows, np.int32))
     ref_o, ref_l = oracle.attention(p, rows=rows)
     gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what="config 4")
+
+
+FP8_VARIANTS = [(32, 8, 128, 16), (8, 2, 64, 16), (16, 8, 256, 32), (64, 8, 64, 64)]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,ps", FP8_VARIANTS)
+@pytest.mark.parametrize("opts", [{}, {"window": 100, "sinks": True}, {"soft_cap": 8.0}])
+def test_extend_fp8_cache(Hq, Hkv, D, ps, opts):
+    # e4m3 cache, dequantised bf16(float(code) * scale) on both sides
+    p = _ext(Hq * 3 + D + ps, Hq=Hq, Hkv=Hkv, D=D, ps=ps, ctx=CTX, ql=QL, kv_dtype="fp8_e4m3",
+             k_scale=0.05, v_scale=0.07, **opts)
+    ref_o, ref_l = oracle.attention(p)
+    out, lse = gh.run(p)
+    gh.assert_parity(out, lse, ref_o, ref_l, what=f"extend fp8 {Hq},{Hkv},{D},{ps} {opts}")
+
+
+def test_extend_fp8_identity_probe_bitwise():
+    for (Hq, Hkv, D, ps) in FP8_VARIANTS:
+        p = _ext(9 + D, Hq=Hq, Hkv=Hkv, D=D, ps=ps, ctx=CTX, ql=QL, kv_dtype="fp8_e4m3", k_scale=0.05,
+                 v_scale=0.05, window=1)
+        out, _ = gh.run(p)
+        ref_o, _ = oracle.attention(p)
+        assert np.array_equal(out.astype(np.float64), ref_o), (Hq, Hkv, D, ps)
