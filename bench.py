@@ -307,6 +307,8 @@ def run_ours(args):
     h2d = hq.numel() * 2 + hbt.numel() * 4 + hsl.numel() * 4
     d2h = hout.numel() * 2 + hlse.numel() * 4
 
+    extras = None if args.no_extras else measure_extras(pb, wl, dp, dd, dev, stream)
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -368,12 +370,80 @@ def run_ours(args):
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "what": "decode through the C ABI: pinned-host q/block_table/seq_lens H2D, pa_plan, pa_decode, out/lse D2H"},
         "gpu_launches": K * ((dplan.launches if decode_on else 0) + (eplan.launches if extend_ok else 0)),
+        "extras": extras,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+# ---- further hot-path modes, timed apart from the step -------------------------------
+
+def _time_calls(torch, fn, stream, n=50, warm=5):
+    for _ in range(warm):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n / 1e3
+
+
+def measure_extras(pb, wl, dp, dd, dev, stream):
+    """Verify mode on the decode workload's sequences (3 speculative tokens per
+    request, K/V of the new tokens already in the pages) and extend with an
+    e4m3 KV cache on the extend workload."""
+    import dataclasses
+    import torch
+    peaks, _ = load_peaks()
+    res = {}
+    # verify: q_len = 4 per request over the decode workload's cache
+    q_len = 4
+    B, Hq, D = dp.batch, dp.num_q_heads, dp.head_dim
+    g = torch.Generator(device="cpu").manual_seed(4242)
+    qv = torch.randn(B * q_len, Hq, D, generator=g).to(torch.bfloat16).to(dev)
+    qsl = torch.arange(0, B * q_len + 1, q_len, dtype=torch.int32, device=dev)
+    vplan = pb.plan(mode=pb.MODE_VERIFY, num_q_heads=Hq, num_kv_heads=dp.num_kv_heads, head_dim=D,
+                    page_size=dp.page_size, max_batch=B, max_pages_per_seq=dp.block_table.shape[1],
+                    max_total_q=B * q_len, q_len=q_len, host_seq_lens=dp.seq_lens)
+    vscr = pb.alloc_scratch(vplan, dev)
+    vout = torch.empty_like(qv)
+    vlse = torch.empty(qv.shape[:2], dtype=torch.float32, device=dev)
+    t = _time_calls(torch, lambda: pb.extend(vplan, qv, dd["k"], dd["v"], dd["bt"], dd["sl"], qsl, scale=dp.scale,
+                                             out=vout, lse=vlse, scratch=vscr, stream=stream), stream)
+    vb = decode_bytes(dp) + B * Hq * D * 2 * 2 * (q_len - 1)
+    res["verify"] = {"workload": "decode workload's sequences, q_len 4 per request (3 speculative tokens)",
+                     "ms": round(t * 1e3, 4), "kv_read_tbs": round(vb / t / 1e12, 4),
+                     "frac_of_hbm": round(vb / t / 1e9 / float(peaks.get("hbm_gbs", 6800.0)), 4),
+                     "device_error": pb.check(vscr)}
+    # extend with an e4m3 cache
+    ep8 = wl.config_problem(EXTEND_CFG, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05)
+
+    def t8(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    e8 = {k: t8(getattr(ep8, a)) for k, a in (("q", "q"), ("k", "k_cache"), ("v", "v_cache"), ("bt", "block_table"),
+                                             ("sl", "seq_lens"), ("qsl", "query_start_loc"))}
+    eplan8 = pb.plan(mode=pb.MODE_EXTEND, num_q_heads=ep8.num_q_heads, num_kv_heads=ep8.num_kv_heads,
+                     head_dim=ep8.head_dim, page_size=ep8.page_size, kv_dtype=pb.KV_FP8_E4M3, max_batch=ep8.batch,
+                     max_pages_per_seq=ep8.block_table.shape[1], max_total_q=ep8.num_rows)
+    escr8 = pb.alloc_scratch(eplan8, dev)
+    eout8 = torch.empty_like(e8["q"])
+    t = _time_calls(torch, lambda: pb.extend(eplan8, e8["q"], e8["k"], e8["v"], e8["bt"], e8["sl"], e8["qsl"],
+                                             scale=ep8.scale, out=eout8, k_scale=ep8.k_scale, v_scale=ep8.v_scale,
+                                             scratch=escr8, stream=stream), stream)
+    fl = extend_flops(ep8)
+    res["extend_fp8"] = {"workload": "extend workload with an e4m3 KV cache (scales 0.05)", "ms": round(t * 1e3, 4),
+                         "tflops": round(fl / t / 1e12, 2),
+                         "frac_of_bf16_peak": round(fl / t / 1e12 / float(peaks.get("bf16_tflops", 1900.0)), 4),
+                         "device_error": pb.check(escr8)}
+    return res
 
 
 # ---- CPU oracle legs --------------------------------------------------------------
@@ -441,6 +511,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-sample", type=int, default=64, help="decode requests in the CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the verify / fp8-extend measurements")
     ap.add_argument("--only", choices=["decode", "extend"], default=None,
                     help="run one of the two calls per step (profiling of reduced cases)")
     ap.add_argument("--decode-batch", type=int, default=None, help="keep the first N decode requests")

@@ -91,6 +91,12 @@ def lib():
             L.oracle_e4m3_to_double.restype = ctypes.c_double
             L.oracle_fp8_dequant.argtypes = [ctypes.c_uint8, ctypes.c_float]
             L.oracle_fp8_dequant.restype = ctypes.c_double
+            L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+            L.oracle_e4m3_encode.restype = ctypes.c_uint8
+            vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+            L.oracle_append_kv.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, i64, i32, i32, vp, i32, i32, i32,
+                                           i32, ctypes.c_float, ctypes.c_float]
+            L.oracle_append_kv.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -105,6 +111,28 @@ def e4m3_to_double(code: int) -> float:
 
 def fp8_dequant(code: int, scale: float) -> float:
     return lib().oracle_fp8_dequant(int(code), float(scale))
+
+
+def e4m3_encode(y: float) -> int:
+    return int(lib().oracle_e4m3_encode(float(y)))
+
+
+def append_kv(k_new: np.ndarray, v_new: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+              slot_mapping: np.ndarray, k_scale: float = 1.0, v_scale: float = 1.0) -> None:
+    """Write new tokens' K/V (uint16 bf16 bits [T, Hkv, D]) into the caches
+    ([pages, page_size, Hkv, D], uint16 or uint8 e4m3), in place."""
+    L = lib()
+    assert k_new.dtype == np.uint16 and v_new.shape == k_new.shape and k_new.strides == v_new.strides
+    assert k_cache.strides == v_cache.strides and k_cache.dtype == v_cache.dtype
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    ns = _elem_strides(k_new)
+    ks = _elem_strides(k_cache)
+    rc = L.oracle_append_kv(k_new.ctypes.data, v_new.ctypes.data, ns[0], ns[1], k_cache.ctypes.data,
+                            v_cache.ctypes.data, ks[0], ks[1], ks[2], k_cache.shape[0], k_cache.shape[1],
+                            sm.ctypes.data, sm.shape[0], k_new.shape[1], k_new.shape[2],
+                            1 if k_cache.dtype == np.uint8 else 0, float(k_scale), float(v_scale))
+    if rc != 0:
+        raise RuntimeError(f"oracle_append_kv failed with code {rc}")
 
 
 def _elem_strides(a: np.ndarray):

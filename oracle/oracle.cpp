@@ -88,9 +88,80 @@ double fp8_dequant(uint8_t code, float scale) {
   return round_to_bf16(prod);
 }
 
+// Encode a binary32 value as OCP E4M3 ("e4m3fn"), round to nearest with
+// ties to even, saturating to +-448 (the largest finite code) and keeping NaN
+// as S.1111.111.  Written from the format: exponent bias 7, 3 mantissa bits,
+// subnormals 2^-6 * m/8, no infinities.
+uint8_t e4m3_encode(float y) {
+  const uint8_t sign = std::signbit(y) ? 0x80 : 0x00;
+  if (std::isnan(y)) return sign | 0x7F;
+  double a = std::fabs(static_cast<double>(y));
+  if (a >= 448.0) return sign | 0x7E;                       // saturate (also +-inf)
+  auto rne = [](double v) {                                  // round half to even
+    const double f = std::floor(v);
+    const double r = v - f;
+    if (r > 0.5) return f + 1.0;
+    if (r < 0.5) return f;
+    return (std::fmod(f, 2.0) == 0.0) ? f : f + 1.0;
+  };
+  if (a < std::ldexp(1.0, -6)) {                             // subnormal range (and zero)
+    const double m = rne(a / std::ldexp(1.0, -9));           // units of 2^-9; m == 8 is 2^-6
+    return sign | static_cast<uint8_t>(m);
+  }
+  int e;
+  const double fr = std::frexp(a, &e);                       // a = fr * 2^e, fr in [0.5, 1)
+  int ex = e - 1;                                            // a = (1 + f) * 2^ex
+  double m = rne((a / std::ldexp(1.0, ex) - 1.0) * 8.0);
+  (void)fr;
+  if (m >= 8.0) {
+    m = 0.0;
+    ex += 1;
+  }
+  const int code = ((ex + 7) << 3) | static_cast<int>(m);
+  if (code > 0x7E) return sign | 0x7E;
+  return sign | static_cast<uint8_t>(code);
+}
+
 }  // namespace
 
 extern "C" {
+
+uint8_t oracle_e4m3_encode(float y) { return e4m3_encode(y); }
+
+// Append new tokens' K/V into the paged cache, as the b12x backend's
+// do_kv_cache_update hands them to reshape_and_cache_flash: token t goes to
+// page slot_mapping[t] / page_size, slot slot_mapping[t] % page_size (a
+// negative slot is padding and is skipped).  bf16 caches store the values;
+// e4m3 caches store e4m3(float(x) / scale) (binary32 division, then
+// e4m3_encode).  Returns 0, or 1 for a slot outside the pool.
+int oracle_append_kv(const uint16_t* k_new, const uint16_t* v_new, int64_t new_stride_tok, int64_t new_stride_head,
+                     void* k_cache, void* v_cache, int64_t kv_stride_page, int64_t kv_stride_tok,
+                     int64_t kv_stride_head, int num_pages, int page_size, const int64_t* slot_mapping,
+                     int num_tokens, int num_kv_heads, int head_dim, int kv_fp8, float k_scale, float v_scale) {
+  for (int t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    const int64_t page = slot / page_size;
+    const int64_t off = slot % page_size;
+    if (page >= num_pages) return 1;
+    for (int h = 0; h < num_kv_heads; ++h) {
+      for (int d = 0; d < head_dim; ++d) {
+        const int64_t src = t * new_stride_tok + h * new_stride_head + d;
+        const int64_t dst = page * kv_stride_page + off * kv_stride_tok + h * kv_stride_head + d;
+        if (kv_fp8) {
+          const float kx = static_cast<float>(bf16_bits_to_double(k_new[src]));
+          const float vx = static_cast<float>(bf16_bits_to_double(v_new[src]));
+          static_cast<uint8_t*>(k_cache)[dst] = e4m3_encode(kx / k_scale);
+          static_cast<uint8_t*>(v_cache)[dst] = e4m3_encode(vx / v_scale);
+        } else {
+          static_cast<uint16_t*>(k_cache)[dst] = k_new[src];
+          static_cast<uint16_t*>(v_cache)[dst] = v_new[src];
+        }
+      }
+    }
+  }
+  return 0;
+}
 
 // Problem description shared with the Python test wrapper (plain C layout).
 // Strides are in ELEMENTS of the respective arrays.

@@ -338,3 +338,74 @@ def test_bad_block_table_rejected(oracle_lib):
     p.block_table[0, 1] = p.num_pages + 3
     with pytest.raises(RuntimeError):
         oracle.attention(p)
+
+
+# ---- the cache write side: e4m3 encoding and KV append ----------------------------
+
+def test_e4m3_encode_roundtrips_every_code(oracle_lib):
+    for c in range(256):
+        if c in (0x7F, 0xFF):
+            continue
+        assert oracle.e4m3_encode(oracle.e4m3_to_double(c)) == c, hex(c)
+
+
+def test_e4m3_encode_matches_torch_including_ties(oracle_lib):
+    # random values, every representable magnitude, and every midpoint between
+    # neighbours (ties go to the even code), all inside the finite range
+    rng = np.random.default_rng(5)
+    vals = [float(x) for x in rng.uniform(-440, 440, 4000)] + [float(x) for x in rng.standard_normal(4000)]
+    mags = sorted({oracle.e4m3_to_double(c) for c in range(0x7F)})
+    vals += mags + [-m for m in mags] + [(a + b) / 2 for a, b in zip(mags, mags[1:])]
+    x = torch.tensor(vals, dtype=torch.float32)
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(v) for v in x.numpy()], np.uint8)
+    assert np.array_equal(ref, got)
+
+
+def test_e4m3_encode_saturates_and_keeps_nan(oracle_lib):
+    assert oracle.e4m3_encode(1e6) == 0x7E and oracle.e4m3_encode(-1e6) == 0xFE
+    assert oracle.e4m3_encode(float("inf")) == 0x7E and oracle.e4m3_encode(464.0) == 0x7E
+    assert oracle.e4m3_encode(float("nan")) & 0x7F == 0x7F
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_append_kv_rebuilds_generated_cache(oracle_lib, kv):
+    # Appending every token's K/V through the slot mapping reproduces the cache
+    # the generator wrote (generator: torch's conversion; here: the oracle's).
+    lens = [9, 30, 17]
+    extra = dict(kv_dtype=kv, k_scale=0.05, v_scale=0.07) if kv == "fp8_e4m3" else {}
+    base = _problem("decode", seed=131, B=3, Hq=4, Hkv=2, D=16, ps=4, lens=lens, **extra)
+    # bf16 inputs whose quantisation the generator also performed
+    rng = np.random.default_rng(9)
+    ks, vs, slots = [], [], []
+    for b, L in enumerate(lens):
+        kx = wl._to_bf16_bits(rng.standard_normal((L, 2, 16), dtype=np.float32))
+        vx = wl._to_bf16_bits(rng.standard_normal((L, 2, 16), dtype=np.float32))
+        ks.append(kx)
+        vs.append(vx)
+        for t in range(L):
+            slots.append(int(base.block_table[b, t // 4]) * 4 + t % 4)
+    k_new, v_new = np.concatenate(ks), np.concatenate(vs)
+    slots = np.array(slots + [-1, -7], np.int64)        # padding slots are skipped
+    k_new = np.concatenate([k_new, k_new[:2]])
+    v_new = np.concatenate([v_new, v_new[:2]])
+    kc, vc = np.zeros_like(base.k_cache), np.zeros_like(base.v_cache)
+    oracle.append_kv(k_new, v_new, kc, vc, slots, 0.05, 0.07)
+    # reference: torch-based cache writes of the same values
+    kr, vr = np.zeros_like(kc), np.zeros_like(vc)
+    f32 = refs.bf16_bits_to_f64(k_new).float()
+    g32 = refs.bf16_bits_to_f64(v_new).float()
+    for t, s in enumerate(slots):
+        if s < 0:
+            continue
+        if kv == "fp8_e4m3":
+            kr[s // 4, s % 4] = (f32[t] / torch.tensor(0.05, dtype=torch.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            vr[s // 4, s % 4] = (g32[t] / torch.tensor(0.07, dtype=torch.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        else:
+            kr[s // 4, s % 4] = k_new[t]
+            vr[s // 4, s % 4] = v_new[t]
+    assert np.array_equal(kc, kr) and np.array_equal(vc, vr)
+    bad = slots.copy()
+    bad[0] = kc.shape[0] * 4
+    with pytest.raises(RuntimeError):
+        oracle.append_kv(k_new, v_new, kc, vc, bad)
