@@ -200,6 +200,26 @@ pa_status pa_extend(const pa_plan_t* plan,
                     float* lse,
                     void* scratch, int64_t scratch_bytes, void* stream);
 
+/* Append new tokens' K and V to the paged cache -- the write side the
+ * attention calls read ("vllm/v1/attention/backends/b12x",
+ * do_kv_cache_update, which passes these arguments to reshape_and_cache_flash).
+ *   k_new, v_new   device bf16 [num_tokens, Hkv, head_dim], strides
+ *                  new_stride_tok / new_stride_head (16-byte aligned rows)
+ *   k_cache, v_cache, kv strides, num_pages, page_size   as for pa_decode
+ *   slot_mapping   device int64 [num_tokens]: token t goes to page
+ *                  slot / page_size, slot slot % page_size; negative = padding, skipped
+ *   kv_dtype       PA_KV_BF16 stores the values; PA_KV_FP8_E4M3 stores
+ *                  e4m3(x / scale) (round to nearest even, saturated to +-448)
+ *   scratch        optional (may be NULL): a scratch buffer whose error header
+ *                  records slots outside the pool (those tokens are not written)
+ * Asynchronous on `stream`; one kernel launch. */
+pa_status pa_append_kv(const void* k_new, const void* v_new, int64_t new_stride_tok, int64_t new_stride_head,
+                       void* k_cache, void* v_cache,
+                       int64_t kv_stride_page, int64_t kv_stride_tok, int64_t kv_stride_head,
+                       int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t kv_dtype, const int64_t* slot_mapping, int32_t num_tokens,
+                       float k_scale, float v_scale, void* scratch, void* stream);
+
 /* Zero the 256-byte error header at the start of a scratch buffer (enqueued
  * on `stream`).  Call once after allocating the scratch. */
 pa_status pa_scratch_init(void* scratch, void* stream);

@@ -28,7 +28,7 @@ KV_BF16 = 0
 KV_FP8_E4M3 = 1
 
 EXPORTED_SYMBOLS = ("pa_plan", "pa_decode", "pa_extend", "pa_scratch_init", "pa_check",
-                    "pa_status_string", "pa_version", "pa_decode_static_scratch")
+                    "pa_status_string", "pa_version", "pa_decode_static_scratch", "pa_append_kv")
 
 
 class PaShape(ctypes.Structure):
@@ -99,6 +99,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.pa_decode_static_scratch.argtypes = [ctypes.POINTER(PaPlan), vp, i64, i64, vp, vp, i64, i64, i64, i32,
                                            vp, i64, vp, i32, f32, vp, f32, f32, vp, i64, i64, vp, vp]
     L.pa_decode_static_scratch.restype = ctypes.c_int
+    L.pa_append_kv.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, f32,
+                               vp, vp]
+    L.pa_append_kv.restype = ctypes.c_int
     L.pa_scratch_init.argtypes = [vp, vp]
     L.pa_scratch_init.restype = ctypes.c_int
     L.pa_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -195,6 +198,19 @@ def decode_static_scratch(p: PaPlan, q, k_cache, v_cache, block_table, seq_lens,
         float(scale), _ptr(sinks), float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1),
         _ptr(lse), _stream(stream))
     _check(status, "pa_decode_static_scratch")
+
+
+def append_kv(k_new, v_new, k_cache, v_cache, slot_mapping, *, kv_dtype: int = KV_BF16, k_scale: float = 1.0,
+              v_scale: float = 1.0, scratch=None, stream=None):
+    """pa_append_kv: write new tokens' K/V (bf16 [T, Hkv, D]) into the paged caches at slot_mapping (int64)."""
+    sp, st, sh = _kv_strides(k_cache, v_cache)
+    if tuple(k_new.stride()) != tuple(v_new.stride()) or k_new.shape != v_new.shape:
+        raise ValueError("k_new and v_new must share shape and strides")
+    status = load().pa_append_kv(
+        _ptr(k_new), _ptr(v_new), k_new.stride(0), k_new.stride(1), _ptr(k_cache), _ptr(v_cache), sp, st, sh,
+        k_cache.shape[0], k_cache.shape[1], k_cache.shape[2], k_cache.shape[3], int(kv_dtype), _ptr(slot_mapping),
+        k_new.shape[0], float(k_scale), float(v_scale), _ptr(scratch), _stream(stream))
+    _check(status, "pa_append_kv")
 
 
 def scratch_init(scratch, stream=None):
