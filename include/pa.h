@@ -75,7 +75,7 @@ typedef enum { PA_MODE_DECODE = 0, PA_MODE_EXTEND = 1, PA_MODE_VERIFY = 2 } pa_m
  * optional host seq_lens hint given to pa_plan). */
 typedef struct {
   int32_t mode;               /* pa_mode */
-  int32_t num_q_heads;        /* Hq; Hq % Hkv == 0 and Hq / Hkv <= 16 */
+  int32_t num_q_heads;        /* Hq; Hq % Hkv == 0 and Hq / Hkv <= 128 */
   int32_t num_kv_heads;       /* Hkv */
   int32_t head_dim;           /* D in {64, 128, 256} */
   int32_t page_size;          /* ps in {16, 32, 64} */

@@ -53,7 +53,9 @@ pa_status validate_shape(const pa_shape& s) {
   if (s.has_sinks != 0 && s.has_sinks != 1) return PA_ERR_INVALID_ARG;
   if (s.head_dim != 64 && s.head_dim != 128 && s.head_dim != 256) return PA_ERR_UNSUPPORTED;
   if (s.page_size != 16 && s.page_size != 32 && s.page_size != 64) return PA_ERR_UNSUPPORTED;
-  if (s.num_q_heads / s.num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
+  // decode splits larger groups over several CTAs (16 heads each); extend
+  // packs 128 / group tokens per query tile
+  if (s.num_q_heads / s.num_kv_heads > 128) return PA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(s.max_pages_per_seq) * s.page_size > (int64_t{1} << 30)) return PA_ERR_UNSUPPORTED;
   if (s.mode == PA_MODE_VERIFY) {
     if (s.q_len < 1) return PA_ERR_INVALID_ARG;
@@ -64,6 +66,12 @@ pa_status validate_shape(const pa_shape& s) {
 
 // Query tokens per request on the split-KV path.
 int split_kv_qlen(const pa_shape& s) { return s.mode == PA_MODE_VERIFY ? s.q_len : 1; }
+
+// CTAs per kv head on the split-KV path: each covers at most 16 query rows.
+int split_kv_head_groups(const pa_shape& s) {
+  const int G = s.num_q_heads / s.num_kv_heads;
+  return (s.mode == PA_MODE_DECODE && G > 16) ? (G + 15) / 16 : 1;
+}
 
 namespace {
 
@@ -76,7 +84,8 @@ int64_t decode_keys(int64_t L, int window, int q_len) {
 pa_status plan_decode(const pa_shape& s, const int32_t* host_lens, int32_t batch, int num_sms, pa_plan_t* out) {
   const int G = s.num_q_heads / s.num_kv_heads;
   const int qlen = split_kv_qlen(s);
-  const int rows = G * qlen;
+  const int hgroups = split_kv_head_groups(s);
+  const int rows = hgroups > 1 ? 16 : G * qlen;
   const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
   DecodeConfig cfg = decode_config(s.head_dim, fp8, rows, 0);
   const int TS = cfg.tile_tokens;
@@ -96,9 +105,9 @@ pa_status plan_decode(const pa_shape& s, const int32_t* host_lens, int32_t batch
         const int64_t n = decode_keys(L, s.window, qlen);
         if (n > 0) units += cdiv64(L, TS) - (L - n) / TS;
       }
-      units *= s.num_kv_heads;
+      units *= static_cast<int64_t>(s.num_kv_heads) * hgroups;
     } else {
-      units = static_cast<int64_t>(s.max_batch) * s.num_kv_heads * max_tiles;
+      units = static_cast<int64_t>(s.max_batch) * s.num_kv_heads * hgroups * max_tiles;
     }
     const int ctas_per_sm = (decode_config(s.head_dim, fp8, rows, 64).smem_bytes * 2 <= kMaxSmemPerCta) ? 2 : 1;
     const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm * 4;
@@ -120,7 +129,7 @@ pa_status plan_decode(const pa_shape& s, const int32_t* host_lens, int32_t batch
   out->bt_cache = static_cast<int32_t>(bt_cache);
   out->smem_bytes = cfg.smem_bytes;
   out->grid[0] = static_cast<int32_t>(max_splits);
-  out->grid[1] = s.num_kv_heads;
+  out->grid[1] = s.num_kv_heads * hgroups;
   out->grid[2] = s.max_batch;
   const int64_t prow = static_cast<int64_t>(s.max_batch) * qlen * s.num_q_heads * max_splits;
   out->scratch_bytes = kScratchHeaderBytes + align_up(prow * s.head_dim * 4, 256) + align_up(prow * 4, 256);
@@ -292,7 +301,8 @@ pa_status run_split_kv(const pa_plan_t* plan, const void* q, int64_t q_stride_to
   const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
   const int G = s.num_q_heads / s.num_kv_heads;
   const int qlen = split_kv_qlen(s);
-  const DecodeConfig cfg = decode_config(s.head_dim, fp8, G * qlen, plan->bt_cache);
+  const int hgroups = split_kv_head_groups(s);
+  const DecodeConfig cfg = decode_config(s.head_dim, fp8, hgroups > 1 ? 16 : G * qlen, plan->bt_cache);
   const int box_rows = std::min(s.page_size, plan->tile_tokens);
   CUtensorMap tmk, tmv;
   if ((st = make_kv_map(&tmk, k_cache, fp8, s.head_dim, s.num_kv_heads, s.page_size, num_pages, kv_stride_page,
@@ -335,9 +345,10 @@ pa_status run_split_kv(const pa_plan_t* plan, const void* q, int64_t q_stride_to
   p.fixed_splits = s.num_splits > 0 ? plan->max_splits : 0;
   p.bt_cache = plan->bt_cache;
   p.q_len = qlen;
+  p.head_groups = hgroups;
   p.qsl = qsl;
   p.err = reinterpret_cast<uint32_t*>(sc);
-  const dim3 grid(plan->max_splits, s.num_kv_heads, batch);
+  const dim3 grid(plan->max_splits, s.num_kv_heads * hgroups, batch);
   const cudaError_t e = launch_decode(cfg, tmk, tmv, p, grid, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -104,7 +104,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
                     const DecodeParams p) {
   using T = Traits<D, FP8, NH8, TS, NS>;
   const int split = blockIdx.x;
-  const int kvh = blockIdx.y;
+  const int kvh = blockIdx.y / p.head_groups;   // kv head; groups above 16 heads use several CTAs
+  const int hg = blockIdx.y - kvh * p.head_groups;
   const int b = blockIdx.z;
   const int L = p.seq_lens[b];
   const SplitRange r = split_range(p, L);
@@ -128,7 +129,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
   const int pg0 = (tile_begin * TS) / ps;
   const int pg1 = (tok_hi + ps - 1) / ps;   // <= ceil(L / ps): never past the request's pages
   const int G = p.group;
-  const int R = p.q_len * G;          // query rows per kv head: (token, head) pairs
+  const int head0 = hg * 16;          // first head (within the kv head's group) of this CTA
+  const int Gc = p.head_groups > 1 ? min(16, G - head0) : G;   // heads this CTA covers
+  const int R = p.q_len * Gc;         // query rows: (token, head) pairs
   // tiles where every row sees every key need no per-element mask
   const int pos_first = L - p.q_len;  // position of the first query
   const int lo_last = p.window > 0 ? (L - 1) - p.window + 1 : 0;
@@ -194,8 +197,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     for (int j = 0; j < NH8; ++j) {
       const int rr = j * 8 + g;   // row = token * G + head
       const bool ok = rr < R;
-      const int tq = ok ? rr / G : 0;
-      const int hq = ok ? rr - tq * G : 0;
+      const int tq = ok ? rr / Gc : 0;
+      const int hq = ok ? head0 + rr - tq * Gc : 0;
       const uint16_t* qh = p.q + static_cast<int64_t>(qrow0 + tq) * p.q_stride_tok +
                            static_cast<int64_t>(kvh * G + hq) * p.q_stride_head;
 #pragma unroll
@@ -230,7 +233,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int rr = j * 8 + 2 * c + h;
-      rpos[j][h] = pos_first + min(rr, R - 1) / G;
+      rpos[j][h] = pos_first + min(rr, R - 1) / Gc;
       rlo[j][h] = p.window > 0 ? rpos[j][h] - p.window + 1 : 0;
     }
   }
@@ -499,8 +502,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
       num += wob[h * D + d] * f;
       den += wob[T::HW * D + T::HW + h] * f;
     }
-    const int tq = h / G;
-    const int hq = kvh * G + (h - tq * G);
+    const int tq = h / Gc;
+    const int hq = kvh * G + head0 + (h - tq * Gc);
     const int64_t orow = qrow0 + tq;
     if (direct) {
       float M2 = M, zs = 0.f;

@@ -43,6 +43,7 @@ struct DecodeParams {
   int fixed_splits;           // >0: split count per request (fixed mode)
   int bt_cache;               // block-table entries staged per CTA
   int q_len;                  // query tokens per request: 1 (decode) or 1 + speculative (verify)
+  int head_groups;            // CTAs per kv head: ceil(group / 16) for decode groups above 16, else 1
   const int32_t* qsl;         // verify: query_start_loc, checked to be b * q_len; null for decode
   uint32_t* err;              // scratch header error word
 };

@@ -74,7 +74,7 @@ def test_plan_fixed_splits(lib):
     (dict(num_q_heads=30), pb.PA_ERR_INVALID_ARG),         # Hq % Hkv != 0
     (dict(head_dim=96), pb.PA_ERR_UNSUPPORTED),
     (dict(page_size=8), pb.PA_ERR_UNSUPPORTED),
-    (dict(num_q_heads=136, num_kv_heads=8), pb.PA_ERR_UNSUPPORTED),  # group 17
+    (dict(num_q_heads=129 * 8, num_kv_heads=8), pb.PA_ERR_UNSUPPORTED),  # group 129
     (dict(window=-1), pb.PA_ERR_INVALID_ARG),
     (dict(soft_cap=-1.0), pb.PA_ERR_INVALID_ARG),
     (dict(soft_cap=float("inf")), pb.PA_ERR_INVALID_ARG),
@@ -198,3 +198,12 @@ def test_plan_verify_scratch_scales_with_q_len(lib):
     four = _plan(mode=pb.MODE_VERIFY, q_len=4, max_total_q=256, num_splits=4)
     assert four.scratch_bytes > 3 * (one.scratch_bytes - 256)
     assert four.launches == 2
+
+
+def test_plan_decode_large_group_uses_head_groups(lib):
+    p = _plan(num_q_heads=64, num_kv_heads=2)          # group 32: two CTAs of 16 heads per kv head
+    assert p.grid[1] == 2 * 2
+    q = _plan(num_q_heads=40, num_kv_heads=2)          # group 20: 16 + 4
+    assert q.grid[1] == 2 * 2
+    e = _plan(mode=pb.MODE_EXTEND, num_q_heads=128, num_kv_heads=1, max_total_q=512)
+    assert e.launches == 2

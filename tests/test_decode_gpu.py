@@ -41,6 +41,8 @@ VARIANTS = [
     (16, 1, 128, 16, "bf16"),       # group 16: two 8-head MMA columns
     (12, 1, 64, 32, "bf16"),        # group 12: padded heads
     (4, 4, 128, 64, "bf16"),        # group 1 (MHA)
+    (64, 2, 128, 16, "bf16"),       # group 32: two 16-head CTAs per kv head
+    (40, 2, 64, 32, "fp8_e4m3"),    # group 20: 16 + 4 heads
 ]
 
 

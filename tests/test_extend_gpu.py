@@ -41,6 +41,8 @@ VARIANTS = [
     (16, 1, 128, 16),     # group 16
     (8, 8, 64, 32),       # group 1
     (12, 4, 128, 16),     # group 3: 126 of 128 rows used
+    (64, 2, 128, 16),     # group 32: 4 tokens per query tile
+    (128, 1, 64, 32),     # group 128: one token per query tile
 ]
 
 
