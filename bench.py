@@ -103,6 +103,25 @@ def recorded_traffic(kernel: str, files):
     return t.get("dram_bytes_per_launch")
 
 
+# ---- multi-rank aggregation ------------------------------------------------------
+
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of per-rank timings (the slowest rank bounds the
+    job); identity on one process."""
+    import torch
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def weak_scaling_throughput(world: int, steps: int, units_per_step: float, seconds: float) -> float:
+    """Whole-job throughput: every rank processed `steps` steps of the same
+    per-GPU workload; `seconds` is the max over ranks."""
+    return world * steps * units_per_step / max(seconds, 1e-12)
+
+
 # ---- clocks -----------------------------------------------------------------------
 
 class ClockSampler:
@@ -261,14 +280,11 @@ def run_ours(args):
         raise RuntimeError("device error during the timed region")
 
     dec_s, ext_s = sum(dec_ms) / 1e3, sum(ext_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([dec_s, ext_s, loop_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dec_s, ext_s, loop_s = (float(x) for x in t.tolist())
+    dec_s, ext_s, loop_s = max_over_ranks([dec_s, ext_s, loop_s], dist if world > 1 else None, dev)
 
     dbytes = decode_bytes(dp)
     eflops = extend_flops(ep) if extend_ok else 0
-    value_tbs = world * K * dbytes / max(dec_s, 1e-12) / 1e12
+    value_tbs = weak_scaling_throughput(world, K, dbytes, dec_s) / 1e12
 
     # ---- end to end through the public API with host buffers ---------------------
     Ke = min(K, 200)
@@ -299,11 +315,7 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_s = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks([e0.elapsed_time(e1) / 1e3], dist if world > 1 else None, dev)[0]
     h2d = hq.numel() * 2 + hbt.numel() * 4 + hsl.numel() * 4
     d2h = hout.numel() * 2 + hlse.numel() * 4
 
@@ -363,10 +375,10 @@ def run_ours(args):
                                    "max_splits": dplan.max_splits, "stages": dplan.stages}},
         "decode_ms": round(statistics.mean(dec_ms), 4),
         "extend_ms": round(statistics.mean(ext_ms), 4) if extend_ok else None,
-        "extend_tflops": round(world * K * eflops / ext_s / 1e12, 2) if extend_ok else None,
+        "extend_tflops": round(weak_scaling_throughput(world, K, eflops, ext_s) / 1e12, 2) if extend_ok else None,
         "roofline": roof,
         "kernels": kernels,
-        "e2e": {"value": round(world * Ke * dbytes / e2e_s / 1e12, 4), "unit": "TB/s",
+        "e2e": {"value": round(weak_scaling_throughput(world, Ke, dbytes, e2e_s) / 1e12, 4), "unit": "TB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "what": "decode through the C ABI: pinned-host q/block_table/seq_lens H2D, pa_plan, pa_decode, out/lse D2H"},
         "gpu_launches": K * ((dplan.launches if decode_on else 0) + (eplan.launches if extend_ok else 0)),
