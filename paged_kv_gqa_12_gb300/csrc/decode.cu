@@ -126,8 +126,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
   const int tok_lo = max(r.lo, tile_begin * TS);
   const int tok_hi = min(r.hi, tile_end * TS);
   const int ps = p.page_size;
-  const int pg0 = (tile_begin * TS) / ps;
-  const int pg1 = (tok_hi + ps - 1) / ps;   // <= ceil(L / ps): never past the request's pages
+  const int ps_log2 = __ffs(ps) - 1;  // page sizes are powers of two: shifts, no integer division
+  const int pg0 = (tile_begin * TS) >> ps_log2;
+  const int pg1 = (tok_hi + ps - 1) >> ps_log2;   // <= ceil(L / ps): never past the request's pages
   const int G = p.group;
   const int head0 = hg * 16;          // first head (within the kv head's group) of this CTA
   const int Gc = p.head_groups > 1 ? min(16, G - head0) : G;   // heads this CTA covers
@@ -179,8 +180,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     mbar_arrive_expect_tx(&wbar[stage], static_cast<uint32_t>(nb * br * T::ROW * 2));
     for (int j = 0; j < nb; ++j) {
       const int t = t0 + j * br;
-      const int page = bt_s[t / ps - pg0];
-      const int slot = t % ps;
+      const int page = bt_s[(t >> ps_log2) - pg0];
+      const int slot = t & (ps - 1);
 #pragma unroll
       for (int cc = 0; cc < T::NCC; ++cc) {
         const int dst = cc * TS * T::RB + j * br * T::RB;

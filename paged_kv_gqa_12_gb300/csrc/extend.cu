@@ -13,13 +13,17 @@
 //   * Tile = 128 query rows x one kv head: the G q heads of each token are
 //     packed into the MMA M dimension (row = token * G + head), so one K/V
 //     tile feeds all heads that share it.
-//   * Warp roles in a 224-thread CTA: warps 0 and 2 issue TMA (Q once, then
+//   * Warp roles in a 256-thread CTA: warps 0 and 2 issue TMA (Q once, then
 //     the K ring and the V ring: one box per page, page ids from the block
-//     table), warp 1 allocates TMEM and issues tcgen05.mma from one thread,
-//     warps 3-6 run the softmax with one TMEM lane (= one query row) per
-//     thread.  Two CTAs share an SM where TMEM and shared memory allow.
+//     table), warp 1 allocates TMEM and issues the S = Q K^T MMAs, warp 7
+//     issues the O += P V MMAs (one thread each: an MMA issue blocks while
+//     the tensor pipe is busy, so one issuer would hold a ready PV behind the
+//     next tile's QK), warps 3-6 run the softmax with one TMEM lane (= one
+//     query row) per thread.  Two CTAs share an SM where TMEM and shared
+//     memory allow.
 //   * S = Q K^T (M=128, N=BN keys) lands in one of two TMEM buffers, so the
-//     next tile's QK overlaps this tile's softmax; P (bf16) is written back
+//     next tile's QK overlaps this tile's softmax (a buffer is reused once
+//     the PV that read its P has completed); P (bf16) is written back
 //     over S and consumed from TMEM by O += P V (V read MN-major from shared
 //     memory); O stays in TMEM for the whole key loop.
 //   * Online softmax in the log2 domain with lazy rescaling: O and l are
@@ -42,7 +46,7 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 224;     // warps: 0 = Q/K TMA, 1 = MMA, 2 = V TMA, 3-6 = softmax
+constexpr int kThreads = 256;     // warps: 0 = Q/K TMA, 1 = QK MMA, 2 = V TMA, 3-6 = softmax, 7 = PV MMA
 constexpr int kRows = 128;           // MMA M: query rows per tile
 constexpr int kSchedThreads = 1024;
 constexpr int kBuckets = 256;        // work classes for the longest-first order
@@ -219,7 +223,9 @@ struct ExtTraits {
   static constexpr int KV_CHUNK = BN * 128;
   static constexpr int TILE = NCH * KV_CHUNK;        // K (or V) tile
   static constexpr int SMEM_DATA = Q_BYTES + 2 * NST * TILE;  // Q, K ring, V ring
-  static constexpr int SMEM = 1024 + SMEM_DATA + 256;
+  // mbarriers: q_full, six per ring stage, s_full/p_full/o_done pairs; then the TMEM address
+  static constexpr int BAR_BYTES = ((1 + 6 * NST + 6) * 8 + 4 + 15) / 16 * 16;
+  static constexpr int SMEM = 1024 + SMEM_DATA + BAR_BYTES;   // 1024: alignment slack for SW128
   // fp8 cache: the e4m3 tile lands in the second half of the bf16 stage
   // buffer, rows of RB8 bytes (row r under bf16 row r's upper chunks when
   // D >= 128), and is dequantised in place
@@ -312,6 +318,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   const int L = ctx + qlen;
   const int G = p.group;
   const int ps = p.page_size;
+  const int ps_log2 = __ffs(ps) - 1;   // page sizes are powers of two: no integer division in the loops
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -372,11 +379,11 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
 #pragma unroll
       for (int c = 0; c < T::NCH; ++c) tma_load_3d(q_s + c * T::Q_CHUNK, &tmq, c * 64, kvh * G, qs + t0, q_full);
     }
-    const int npg = BN / ps;
+    const int npg = BN >> ps_log2;
     // page coordinate of this lane's page of key tile j; pages with no
     // attended key are fetched out of bounds, where TMA writes zeros
     auto page_coord = [&](int j) {
-      const int pg = ((kt0 + j) * BN) / ps + lane;
+      const int pg = (((kt0 + j) * BN) >> ps_log2) + lane;
       const bool outside = (pg * ps >= L) || ((pg + 1) * ps <= lo_min);
       return outside ? p.num_pages : bt_row[pg];
     };
@@ -429,65 +436,69 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer (one thread) ----------------
+    // ---------------- S = Q K^T issuer (one thread) ----------------
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(kRows, BN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(kRows, D, false, true);
       const uint32_t q_u = smem_u32(q_s);
       const uint32_t k_ring = smem_u32(k_s);
+      bool ok = wait_or_abort(q_full, 0, p.err);
+      tc_fence_after();
+      for (int j = 0; j < n && ok; ++j) {
+        const int stage = j % NST;
+        ok = wait_or_abort(&k_full[stage], (j / NST) & 1, p.err);
+        // S buffer j & 1 holds P of tile j - 2 until the PV that reads it has completed
+        if (ok && j >= 2) ok = wait_or_abort(&o_done[j & 1], ((j - 2) >> 1) & 1, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tS = tbase + static_cast<uint32_t>((j & 1) * BN);
+        const uint32_t k_u = k_ring + stage * T::TILE;
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s) {
+          const uint64_t ad = sdesc_sw128(q_u + (s >> 2) * T::Q_CHUNK + (s & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(k_u + (s >> 2) * T::KV_CHUNK + (s & 3) * 32, 16, 1024);
+          umma_ss(tS, ad, bd, idesc_qk, s > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[j & 1]);
+        umma_commit(&k_empty[stage]);
+      }
+    }
+  } else if (warp == 7) {
+    // ---------------- O += P V issuer (one thread) ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_pv = idesc_bf16(kRows, D, false, true);
       const uint32_t v_ring = smem_u32(v_s);
       const int pos_min = ctx + t0;
       const int lo_max = p.window > 0 ? ctx + t_end - 1 - p.window + 1 : 0;
-      bool ok = wait_or_abort(q_full, 0, p.err);
-      tc_fence_after();
-      for (int j = 0; j <= n && ok; ++j) {
-        if (j < n) {
-          const int stage = j % NST;
-          ok = wait_or_abort(&k_full[stage], (j / NST) & 1, p.err);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t tS = tbase + static_cast<uint32_t>((j & 1) * BN);
-          const uint32_t k_u = k_ring + stage * T::TILE;
+      bool ok = true;
+      for (int jj = 0; jj < n && ok; ++jj) {
+        const int st = jj % NST;
+        ok = wait_or_abort(&p_full[jj & 1], (jj >> 1) & 1, p.err) &&
+             wait_or_abort(&v_full[st], (jj / NST) & 1, p.err);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tP = tbase + static_cast<uint32_t>((jj & 1) * BN);
+        const uint32_t v_u = v_ring + st * T::TILE;
+        // P columns: k-step s (16 keys) at column 8s; on split tiles P_hi at
+        // 16s and P_lo at 16s + 8
+        const bool split = split_p_tile((kt0 + jj) * BN, BN, pos_min, lo_max, L);
+        const uint32_t pstep = split ? 16u : 8u;
 #pragma unroll
-          for (int s = 0; s < D / 16; ++s) {
-            const uint64_t ad = sdesc_sw128(q_u + (s >> 2) * T::Q_CHUNK + (s & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(k_u + (s >> 2) * T::KV_CHUNK + (s & 3) * 32, 16, 1024);
-            umma_ss(tS, ad, bd, idesc_qk, s > 0 ? 1u : 0u);
-          }
-          umma_commit(&s_full[j & 1]);
-          umma_commit(&k_empty[stage]);
+        for (int s = 0; s < BN / 16; ++s) {
+          const uint64_t bd = sdesc_sw128(v_u + s * 16 * 128, T::KV_CHUNK, 1024);
+          umma_ts(tbase + T::TMEM_O, tP + s * pstep, bd, idesc_pv, (jj > 0 || s > 0) ? 1u : 0u);
         }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const int st = jj % NST;
-          ok = wait_or_abort(&p_full[jj & 1], (jj >> 1) & 1, p.err) &&
-               wait_or_abort(&v_full[st], (jj / NST) & 1, p.err);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t tP = tbase + static_cast<uint32_t>((jj & 1) * BN);
-          const uint32_t v_u = v_ring + st * T::TILE;
-          // P columns: k-step s (16 keys) at column 8s; on split tiles P_hi at
-          // 16s and P_lo at 16s + 8
-          const bool split = split_p_tile((kt0 + jj) * BN, BN, pos_min, lo_max, L);
-          const uint32_t pstep = split ? 16u : 8u;
+        if (split) {
 #pragma unroll
           for (int s = 0; s < BN / 16; ++s) {
             const uint64_t bd = sdesc_sw128(v_u + s * 16 * 128, T::KV_CHUNK, 1024);
-            umma_ts(tbase + T::TMEM_O, tP + s * pstep, bd, idesc_pv, (jj > 0 || s > 0) ? 1u : 0u);
+            umma_ts(tbase + T::TMEM_O, tP + s * 16 + 8, bd, idesc_pv, 1u);
           }
-          if (split) {
-#pragma unroll
-            for (int s = 0; s < BN / 16; ++s) {
-              const uint64_t bd = sdesc_sw128(v_u + s * 16 * 128, T::KV_CHUNK, 1024);
-              umma_ts(tbase + T::TMEM_O, tP + s * 16 + 8, bd, idesc_pv, 1u);
-            }
-          }
-          umma_commit(&o_done[jj & 1]);
-          umma_commit(&v_empty[st]);
         }
+        umma_commit(&o_done[jj & 1]);
+        umma_commit(&v_empty[st]);
       }
     }
-  } else if (warp >= 3) {
+  } else {
     // ---------------- softmax warpgroup: one query row per thread ----------------
     // warps 3-6 cover the four TMEM lane quarters (a warp may only access
     // lanes 32 * (warp % 4) .. + 31)
@@ -502,6 +513,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     const bool capped = p.cap_log2 > 0.f;
     const bool plain = !capped && p.scale_log2 > 0.f;
     const int lo_max_cta = p.window > 0 ? ctx + t_end - 1 - p.window + 1 : 0;
+    const int l_pad = ((L + ps - 1) >> ps_log2) << ps_log2;   // end of the last page
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
@@ -618,7 +630,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         tmem_wait_st();
       }
       // value rows past the sequence end inside the last page of this tile
-      const int pend = min(k0 + BN, ((L + ps - 1) / ps) * ps);
+      const int pend = min(k0 + BN, l_pad);
       if (L < pend) {
         // V of this tile must have landed before its rows are overwritten
         ok = __all_sync(0xffffffffu, wait_or_abort(&v_full[j % NST], (j / NST) & 1, p.err));
