@@ -284,7 +284,8 @@ def run_ours(args):
 
     dbytes = decode_bytes(dp)
     eflops = extend_flops(ep) if extend_ok else 0
-    value_tbs = weak_scaling_throughput(world, K, dbytes, dec_s) / 1e12
+    # --only extend (profiling runs) times no decode: no decode value
+    value_tbs = weak_scaling_throughput(world, K, dbytes, dec_s) / 1e12 if decode_on else None
 
     # ---- end to end through the public API with host buffers ---------------------
     Ke = min(K, 200)
@@ -306,16 +307,18 @@ def run_ours(args):
         hout.copy_(dout, non_blocking=True)
         hlse.copy_(dlse, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    barrier()
-    e0.record(stream)
-    for _ in range(Ke):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_s = max_over_ranks([e0.elapsed_time(e1) / 1e3], dist if world > 1 else None, dev)[0]
+    e2e_s = None
+    if decode_on:
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        e0.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_s = max_over_ranks([e0.elapsed_time(e1) / 1e3], dist if world > 1 else None, dev)[0]
     h2d = hq.numel() * 2 + hbt.numel() * 4 + hsl.numel() * 4
     d2h = hout.numel() * 2 + hlse.numel() * 4
 
@@ -329,15 +332,15 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     bf16 = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    dec_mean = statistics.mean(dec_ms) / 1e3
-    dec_ach = dbytes / dec_mean / 1e9
-    kernels = {
-        "decode": {"bound": "hbm", "achieved": round(dec_ach, 1), "peak": hbm, "unit": "GB/s",
-                   "frac": round(dec_ach / hbm, 4),
-                   "traffic": recorded_traffic("decode_split_kernel", ["decode.cu", "ptx.cuh", "pa_internal.h"]),
-                   "timed": "pa_decode call (split kernel + merge kernel), CUDA events, mean over steps",
-                   "algorithmic_bytes_per_launch": dbytes, "peak_source": f"{peak_src} hbm_gbs"},
-    }
+    kernels = {}
+    if decode_on:
+        dec_mean = statistics.mean(dec_ms) / 1e3
+        dec_ach = dbytes / dec_mean / 1e9
+        kernels["decode"] = {"bound": "hbm", "achieved": round(dec_ach, 1), "peak": hbm, "unit": "GB/s",
+                             "frac": round(dec_ach / hbm, 4),
+                             "traffic": recorded_traffic("decode_split_kernel", ["decode.cu", "ptx.cuh", "pa_internal.h"]),
+                             "timed": "pa_decode call (split kernel + merge kernel), CUDA events, mean over steps",
+                             "algorithmic_bytes_per_launch": dbytes, "peak_source": f"{peak_src} hbm_gbs"}
     if extend_ok:
         ext_mean = statistics.mean(ext_ms) / 1e3
         ext_ach = eflops / ext_mean / 1e12
@@ -346,8 +349,8 @@ def run_ours(args):
                              "traffic": recorded_traffic("extend_attn_kernel", ["extend.cu", "ptx.cuh", "tcgen05.cuh", "pa_internal.h"]),
                              "timed": "pa_extend call (scheduler + attention kernel), CUDA events, mean over steps",
                              "algorithmic_flops_per_launch": eflops, "peak_source": f"{peak_src} bf16_tflops (burst)"}
-    dominant = "decode"
-    if extend_ok and statistics.mean(ext_ms) > statistics.mean(dec_ms):
+    dominant = "decode" if decode_on else "extend"
+    if decode_on and extend_ok and statistics.mean(ext_ms) > statistics.mean(dec_ms):
         dominant = "extend"
     roof = {k: v for k, v in kernels[dominant].items() if k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
     roof["kernel"] = dominant
@@ -356,7 +359,7 @@ def run_ours(args):
     clocks = sampler.summary(t0, t1) if sampler else None
     line = {
         "metric": "paged decode KV-read TB/s (% of HBM peak); extend TFLOP/s (% bf16 peak)",
-        "value": round(value_tbs, 4),
+        "value": round(value_tbs, 4) if value_tbs is not None else None,
         "unit": "TB/s",
         "n_gpus": world,
         "steps": K,
@@ -373,14 +376,15 @@ def run_ours(args):
                    "l2": "not flushed: each step streams > 1.2 GB (L2 129 MB) in a fixed order",
                    "decode_plan": {"tile_tokens": dplan.tile_tokens, "split_tiles": dplan.split_tiles,
                                    "max_splits": dplan.max_splits, "stages": dplan.stages}},
-        "decode_ms": round(statistics.mean(dec_ms), 4),
+        "decode_ms": round(statistics.mean(dec_ms), 4) if decode_on else None,
         "extend_ms": round(statistics.mean(ext_ms), 4) if extend_ok else None,
         "extend_tflops": round(weak_scaling_throughput(world, K, eflops, ext_s) / 1e12, 2) if extend_ok else None,
         "roofline": roof,
         "kernels": kernels,
         "e2e": {"value": round(weak_scaling_throughput(world, Ke, dbytes, e2e_s) / 1e12, 4), "unit": "TB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "what": "decode through the C ABI: pinned-host q/block_table/seq_lens H2D, pa_plan, pa_decode, out/lse D2H"},
+                "what": "decode through the C ABI: pinned-host q/block_table/seq_lens H2D, pa_plan, pa_decode, out/lse D2H"}
+               if e2e_s is not None else None,
         "gpu_launches": K * ((dplan.launches if decode_on else 0) + (eplan.launches if extend_ok else 0)),
         "extras": extras,
         "clocks": clocks,

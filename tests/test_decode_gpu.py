@@ -56,12 +56,12 @@ def test_decode_variants(Hq, Hkv, D, ps, kv, opts):
         gh.assert_parity(out, lse, ref_o, ref_l, what=f"splits={ns}")
 
 
-def test_config1_split_counts():
+def test_tiny_decode_split_counts():
     p = wl.config_problem(1)
     ref_o, ref_l = oracle.attention(p)
     for ns in (4, 1, 2, 3, 7, 0):
         out, lse = gh.run(p, num_splits=ns)
-        gh.assert_parity(out, lse, ref_o, ref_l, what=f"config1 splits={ns}")
+        gh.assert_parity(out, lse, ref_o, ref_l, what=f"tiny decode, splits={ns}")
 
 
 def test_split_invariance_close():
@@ -147,7 +147,7 @@ def test_no_lse_output():
 
 
 @pytest.mark.parametrize("cid", [2, 3, 5])
-def test_full_size_configs_sampled(cid):
+def test_full_size_decode_workloads_sampled(cid):
     # The benchmark workloads at full size, in the launch configuration the
     # benchmark uses (planner with host lengths); the oracle evaluates a
     # sample of rows one by one.
@@ -157,5 +157,5 @@ def test_full_size_configs_sampled(cid):
     rows = np.unique(np.concatenate([rng.choice(p.batch, size=12, replace=False),
                                      [int(np.argmax(p.seq_lens)), int(np.argmin(p.seq_lens))]])).astype(np.int32)
     ref_o, ref_l = oracle.attention(p, rows=rows)
-    gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what=f"config {cid}")
+    gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what=wl.CONFIG_NAMES[cid])
     assert np.isfinite(out).all() and np.isfinite(lse).all()

@@ -100,7 +100,7 @@ def test_extend_empty_request_rows():
     gh.assert_parity(out, lse, ref_o, ref_l)
 
 
-def test_extend_config4_full_sampled():
+def test_extend_full_size_workload_sampled():
     p = wl.config_problem(4)
     out, lse = gh.run(p)
     assert np.isfinite(out).all() and np.isfinite(lse).all()
@@ -110,7 +110,7 @@ def test_extend_config4_full_sampled():
     rows += list(rng.choice(p.num_rows, size=48, replace=False))
     rows = np.unique(np.array(rows, np.int32))
     ref_o, ref_l = oracle.attention(p, rows=rows)
-    gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what="config 4")
+    gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what="extend workload, full size")
 
 
 FP8_VARIANTS = [(32, 8, 128, 16), (8, 2, 64, 16), (16, 8, 256, 32), (64, 8, 64, 64)]
