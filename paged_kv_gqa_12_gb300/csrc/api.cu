@@ -141,7 +141,7 @@ pa_status plan_decode(const pa_shape& s, const int32_t* host_lens, int32_t batch
   out->grid[2] = s.max_batch;
   const int64_t prow = static_cast<int64_t>(s.max_batch) * qlen * s.num_q_heads * max_splits;
   out->scratch_bytes = kScratchHeaderBytes + align_up(prow * s.head_dim * 4, 256) + align_up(prow * 4, 256);
-  out->launches = 2;  // split kernel + merge kernel
+  out->launches = max_splits > 1 ? 2 : 1;  // split kernel (+ merge kernel when a request can have several splits)
   return PA_OK;
 }
 

@@ -109,6 +109,26 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
   const int b = blockIdx.z;
   const int L = p.seq_lens[b];
   const SplitRange r = split_range(p, L);
+  if (r.n_splits == 0) {
+    // nothing to attend (an empty request): O = 0, and the LSE is the sink
+    // logit, or -inf without sinks; the first split's CTA writes its rows
+    if (split == 0) {
+      const int G = p.group;
+      const int head0 = hg * 16;
+      const int Gc = p.head_groups > 1 ? min(16, G - head0) : G;
+      const int R = p.q_len * Gc;
+      const int64_t qrow0 = static_cast<int64_t>(b) * p.q_len;
+      for (int i = threadIdx.x; i < R * D; i += blockDim.x) {
+        const int rr = i / D, d = i - rr * D;
+        const int tq = rr / Gc;
+        const int hq = kvh * G + head0 + (rr - tq * Gc);
+        p.out[(qrow0 + tq) * p.out_stride_tok + static_cast<int64_t>(hq) * p.out_stride_head + d] = 0;
+        if (d == 0 && p.lse != nullptr)
+          p.lse[(qrow0 + tq) * p.num_q_heads + hq] = p.sinks != nullptr ? p.sinks[hq] : -INFINITY;
+      }
+    }
+    return;
+  }
   if (split >= r.n_splits) return;
   if (r.n_splits > p.max_splits) {  // seq_lens beyond the planned capacity
     if (threadIdx.x == 0 && split == 0) atomicOr(p.err, kErrCapacity);
@@ -538,7 +558,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
   const int hq = wid - row * p.num_q_heads;
   const int b = row / p.q_len;
   const SplitRange r = split_range(p, p.seq_lens[b]);
-  if (r.n_splits == 1) return;  // written by the split kernel
+  if (r.n_splits <= 1) return;  // written by the split kernel (no keys, or one split)
   if (r.n_splits > p.max_splits) {  // seq_lens beyond the planned capacity
     if (lane == 0) atomicOr(p.err, kErrCapacity);
     return;
@@ -591,8 +611,10 @@ cudaError_t launch_variant(const CUtensorMap& tmk, const CUtensorMap& tmv, const
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  // with one split per request the split kernel writes the outputs itself
+  // (and flags any request that would need more): no merge launch
   const int warps = p.batch * p.q_len * p.num_q_heads;
-  if (warps > 0) {
+  if (warps > 0 && p.max_splits > 1) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((warps + 3) / 4);
     cfg.blockDim = dim3(128);

@@ -156,9 +156,10 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t bits) {
 __device__ __forceinline__ uint32_t dequant_e4m3x2(uint32_t pair16, float scale) {
   const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair16 & 0xFFFFu),
                                                    __NV_E4M3);
-  const float lo = __fmul_rn(__half2float(__ushort_as_half(h.x)), scale);
-  const float hi = __fmul_rn(__half2float(__ushort_as_half(h.y)), scale);
-  return pack_bf16x2(lo, hi);
+  // both products in one packed fp32x2 multiply (each rounded as __fmul_rn)
+  const float2 f = make_float2(__half2float(__ushort_as_half(h.x)), __half2float(__ushort_as_half(h.y)));
+  const float2 r = __fmul2_rn(f, make_float2(scale, scale));
+  return pack_bf16x2(r.x, r.y);
 }
 
 }  // namespace pa

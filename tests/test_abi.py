@@ -200,6 +200,13 @@ def test_plan_verify_scratch_scales_with_q_len(lib):
     assert four.launches == 2
 
 
+def test_plan_single_split_makes_one_launch(lib):
+    # one split per request: the split kernel writes the outputs, no merge launch
+    one = _plan(num_splits=1)
+    assert one.max_splits == 1 and one.launches == 1
+    assert _plan(num_splits=2).launches == 2
+
+
 def test_plan_decode_large_group_uses_head_groups(lib):
     p = _plan(num_q_heads=64, num_kv_heads=2)          # group 32: two CTAs of 16 heads per kv head
     assert p.grid[1] == 2 * 2
