@@ -105,7 +105,12 @@ typedef struct {
   int32_t grid[3];            /* main kernel grid */
   int64_t scratch_bytes;      /* device scratch the calls need (>= 256) */
   int32_t launches;           /* kernel launches one call makes */
-  int32_t reserved[7];
+  int32_t kv_copy;            /* extend over an e4m3 cache: 1 = each call first dequantises the
+                                 pages it reads, once, into a bf16 copy inside the scratch
+                                 workspace and attends over the copy (chosen while the copy
+                                 for max_batch x max_pages_per_seq pages fits in 2 GiB);
+                                 0 = every attention CTA dequantises its tiles in shared memory */
+  int32_t reserved[6];
 } pa_plan_t;
 
 /* Plan a decode or extend call from capacities.  host_seq_lens (host memory,
@@ -186,7 +191,11 @@ pa_status pa_decode_static_scratch(const pa_plan_t* plan,
  * plan->shape.max_total_q.  With a PA_MODE_VERIFY plan every request must
  * hold exactly plan->shape.q_len rows (query_start_loc[b] = b * q_len,
  * total_q = batch * q_len); the call runs the split-KV kernels and a bad
- * packing sets the device error word.  Other arguments as for pa_decode. */
+ * packing sets the device error word.  With an e4m3 cache and plan->kv_copy
+ * the call first writes bf16(float(code) * scale) of every page a request
+ * reads into the scratch workspace (pages before the sliding window are
+ * skipped) and attends over that copy; the values the attention sees are the
+ * same either way.  Other arguments as for pa_decode. */
 pa_status pa_extend(const pa_plan_t* plan,
                     const void* q, int64_t q_stride_tok, int64_t q_stride_head,
                     const void* k_cache, const void* v_cache,

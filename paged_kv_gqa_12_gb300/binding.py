@@ -64,7 +64,8 @@ class PaPlan(ctypes.Structure):
         ("grid", ctypes.c_int32 * 3),
         ("scratch_bytes", ctypes.c_int64),
         ("launches", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 7),
+        ("kv_copy", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 6),
     ]
 
 

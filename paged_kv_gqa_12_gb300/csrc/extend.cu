@@ -718,6 +718,87 @@ cudaError_t launch_ext(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUt
   return cudaLaunchKernelEx(&cfg, kern, tmq, tmk, tmv, p);
 }
 
+// e4m3 cache, dequantised once per call: every page a request attends to is
+// written as bf16(float(code) * scale) into a dense copy, page i of request
+// b at copy page b * maxp + i, with an identity block table beside it; the
+// bf16 attention kernel then reads the copy.  Each K/V tile is otherwise
+// dequantised by every query tile of its request.
+struct KvCopyParams {
+  const uint8_t* k;
+  const uint8_t* v;
+  int64_t stride_page, stride_tok, stride_head;   // bytes (e4m3)
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* seq_lens;
+  const int32_t* qsl;
+  int batch, num_pages, page_size, num_kv_heads, window, maxp, max_kv;
+  float k_scale, v_scale;
+  uint16_t* kc;
+  uint16_t* vc;
+  int32_t* bt_copy;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) extend_kv_copy_kernel(const KvCopyParams p) {
+  const int i = blockIdx.x;   // page of the request
+  const int b = blockIdx.y;
+  const int64_t dst_page = static_cast<int64_t>(b) * p.maxp + i;
+  if (threadIdx.x == 0) p.bt_copy[dst_page] = static_cast<int32_t>(dst_page);
+  const int L = p.seq_lens[b];
+  const int qlen = p.qsl[b + 1] - p.qsl[b];
+  const int ctx = L - qlen;
+  // malformed rows are reported by the scheduler; nothing to copy for them
+  if (qlen <= 0 || ctx < 0 || L > p.max_kv) return;
+  const int ps = p.page_size;
+  const int first = p.window > 0 ? max(0, ctx - p.window + 1) : 0;   // first key any query attends
+  if ((i + 1) * ps <= first || i * ps >= L) return;
+  const int src = p.block_table[static_cast<int64_t>(b) * p.bt_stride + i];
+  constexpr int UPH = D / 16;   // 16-code units per head row
+  const int units = ps * p.num_kv_heads * UPH;
+  const int64_t page_elems = static_cast<int64_t>(ps) * p.num_kv_heads * D;
+  uint4* kd = reinterpret_cast<uint4*>(p.kc + dst_page * page_elems);
+  uint4* vd = reinterpret_cast<uint4*>(p.vc + dst_page * page_elems);
+  if (src < 0 || src >= p.num_pages) {
+    // a page id outside the pool reads as zeros, as a TMA box outside it does
+    for (int u = threadIdx.x; u < 2 * units; u += blockDim.x) {
+      kd[u] = make_uint4(0, 0, 0, 0);
+      vd[u] = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+  for (int u = threadIdx.x; u < units; u += blockDim.x) {
+    const int tok = u / (p.num_kv_heads * UPH);
+    const int rem = u - tok * (p.num_kv_heads * UPH);
+    const int head = rem / UPH;
+    const int d16 = rem - head * UPH;
+    const int64_t off = static_cast<int64_t>(src) * p.stride_page + static_cast<int64_t>(tok) * p.stride_tok +
+                        static_cast<int64_t>(head) * p.stride_head + d16 * 16;
+    const uint4 kw = *reinterpret_cast<const uint4*>(p.k + off);
+    const uint4 vw = *reinterpret_cast<const uint4*>(p.v + off);
+    const uint32_t ka[4] = {kw.x, kw.y, kw.z, kw.w};
+    const uint32_t va[4] = {vw.x, vw.y, vw.z, vw.w};
+    uint32_t ko[8], vo[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      ko[2 * k] = dequant_e4m3x2(ka[k] & 0xffffu, p.k_scale);
+      ko[2 * k + 1] = dequant_e4m3x2(ka[k] >> 16, p.k_scale);
+      vo[2 * k] = dequant_e4m3x2(va[k] & 0xffffu, p.v_scale);
+      vo[2 * k + 1] = dequant_e4m3x2(va[k] >> 16, p.v_scale);
+    }
+    kd[2 * u] = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+    kd[2 * u + 1] = make_uint4(ko[4], ko[5], ko[6], ko[7]);
+    vd[2 * u] = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+    vd[2 * u + 1] = make_uint4(vo[4], vo[5], vo[6], vo[7]);
+  }
+}
+
+constexpr int64_t kMaxKvCopyBytes = int64_t{2} << 30;   // bf16 K + V copy of an e4m3 cache
+
+int64_t kv_copy_bytes(const pa_shape& s) {
+  return static_cast<int64_t>(s.max_batch) * s.max_pages_per_seq * s.page_size * s.num_kv_heads * s.head_dim *
+         2 /* bf16 */ * 2 /* K and V */;
+}
+
 // Per head_dim: keys per tile and pipeline stages (shared memory <= 227 KB).
 struct ExtChoice {
   int block_n, stages, smem;
@@ -755,6 +836,14 @@ pa_status plan_extend(const pa_shape& s, int num_sms, pa_plan_t* out) {
   out->grid[2] = 1;
   out->scratch_bytes = kScratchHeaderBytes + align_up(work_cap * 8, 256);
   out->launches = 2;  // scheduler + attention kernel
+  out->kv_copy = 0;
+  if (s.kv_dtype == PA_KV_FP8_E4M3 && kv_copy_bytes(s) <= kMaxKvCopyBytes) {
+    // identity block table, then the bf16 K and V copies
+    out->kv_copy = 1;
+    out->scratch_bytes += align_up(static_cast<int64_t>(s.max_batch) * s.max_pages_per_seq * 4, 256) +
+                          2 * align_up(kv_copy_bytes(s) / 2, 256);
+    out->launches = 3;
+  }
   return PA_OK;
 }
 
@@ -818,25 +907,82 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
   if ((st = make_q_map(&tmq, q, s.head_dim, s.num_q_heads, total_q, q_stride_tok, q_stride_head, G, tm)) !=
       PA_OK)
     return st;
-  if ((st = make_kv_map(&tmk, k_cache, fp8, s.head_dim, s.num_kv_heads, s.page_size, num_pages,
-                               kv_stride_page, kv_stride_tok, kv_stride_head, s.page_size)) != PA_OK)
+  uint8_t* sc = static_cast<uint8_t*>(scratch);
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  const int64_t cap_items = plan->grid[0] / s.num_kv_heads;
+  // e4m3 cache with a copy plan: dequantise the attended pages once into the
+  // scratch workspace (after the work list), then attend over the bf16 copy
+  const bool copy = fp8 && plan->kv_copy != 0 && batch <= 65535;
+  const void* kbase = k_cache;
+  const void* vbase = v_cache;
+  const int32_t* bt = block_table;
+  int64_t bts = bt_stride, st_page = kv_stride_page, st_tok = kv_stride_tok, st_head = kv_stride_head;
+  int32_t pages = num_pages;
+  if (copy) {
+    const int64_t maxp = s.max_pages_per_seq;
+    uint8_t* cbase = sc + kScratchHeaderBytes + align_up(cap_items * 8, 256);
+    int32_t* bt_copy = reinterpret_cast<int32_t*>(cbase);
+    uint8_t* kc = cbase + align_up(static_cast<int64_t>(s.max_batch) * maxp * 4, 256);
+    uint8_t* vc = kc + align_up(kv_copy_bytes(s) / 2, 256);
+    if (static_cast<int64_t>(batch) * maxp > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    KvCopyParams cp{};
+    cp.k = static_cast<const uint8_t*>(k_cache);
+    cp.v = static_cast<const uint8_t*>(v_cache);
+    cp.stride_page = kv_stride_page;
+    cp.stride_tok = kv_stride_tok;
+    cp.stride_head = kv_stride_head;
+    cp.block_table = block_table;
+    cp.bt_stride = bt_stride;
+    cp.seq_lens = seq_lens;
+    cp.qsl = query_start_loc;
+    cp.batch = batch;
+    cp.num_pages = num_pages;
+    cp.page_size = s.page_size;
+    cp.num_kv_heads = s.num_kv_heads;
+    cp.window = s.window;
+    cp.maxp = static_cast<int>(maxp);
+    cp.max_kv = s.max_pages_per_seq * s.page_size;
+    cp.k_scale = k_scale;
+    cp.v_scale = v_scale;
+    cp.kc = reinterpret_cast<uint16_t*>(kc);
+    cp.vc = reinterpret_cast<uint16_t*>(vc);
+    cp.bt_copy = bt_copy;
+    const dim3 cgrid(static_cast<unsigned>(maxp), static_cast<unsigned>(batch));
+    switch (s.head_dim) {
+      case 64: extend_kv_copy_kernel<64><<<cgrid, 256, 0, strm>>>(cp); break;
+      case 128: extend_kv_copy_kernel<128><<<cgrid, 256, 0, strm>>>(cp); break;
+      default: extend_kv_copy_kernel<256><<<cgrid, 256, 0, strm>>>(cp); break;
+    }
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    kbase = kc;
+    vbase = vc;
+    bt = bt_copy;
+    bts = maxp;
+    st_head = s.head_dim;
+    st_tok = static_cast<int64_t>(s.num_kv_heads) * s.head_dim;
+    st_page = st_tok * s.page_size;
+    pages = static_cast<int32_t>(static_cast<int64_t>(batch) * maxp);
+  }
+  const bool fp8_tiles = fp8 && !copy;   // the attention kernel dequantises in shared memory
+  if ((st = make_kv_map(&tmk, kbase, fp8_tiles, s.head_dim, s.num_kv_heads, s.page_size, pages, st_page, st_tok,
+                        st_head, s.page_size)) != PA_OK)
     return st;
-  if ((st = make_kv_map(&tmv, v_cache, fp8, s.head_dim, s.num_kv_heads, s.page_size, num_pages,
-                               kv_stride_page, kv_stride_tok, kv_stride_head, s.page_size)) != PA_OK)
+  if ((st = make_kv_map(&tmv, vbase, fp8_tiles, s.head_dim, s.num_kv_heads, s.page_size, pages, st_page, st_tok,
+                        st_head, s.page_size)) != PA_OK)
     return st;
 
   ExtendParams p{};
   p.seq_lens = seq_lens;
   p.qsl = query_start_loc;
-  p.block_table = block_table;
-  p.bt_stride = bt_stride;
+  p.block_table = bt;
+  p.bt_stride = bts;
   p.batch = batch;
   p.total_q = total_q;
   p.num_q_heads = s.num_q_heads;
   p.num_kv_heads = s.num_kv_heads;
   p.group = G;
   p.page_size = s.page_size;
-  p.num_pages = num_pages;
+  p.num_pages = pages;
   p.tm = tm;
   p.max_kv = s.max_pages_per_seq * s.page_size;
   p.block_n = ch.block_n;
@@ -845,23 +991,20 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
   p.scale_over_cap = s.soft_cap > 0.f ? scale / s.soft_cap : 0.f;
   p.window = s.window;
   p.sinks = sinks;
-  p.k_scale = fp8 ? k_scale : 1.f;
-  p.v_scale = fp8 ? v_scale : 1.f;
+  p.k_scale = fp8_tiles ? k_scale : 1.f;
+  p.v_scale = fp8_tiles ? v_scale : 1.f;
   p.out = static_cast<uint16_t*>(out);
   p.out_stride_tok = out_stride_tok;
   p.out_stride_head = out_stride_head;
   p.lse = lse;
-  uint8_t* sc = static_cast<uint8_t*>(scratch);
   p.err = reinterpret_cast<uint32_t*>(sc);
   p.work_count = reinterpret_cast<int*>(sc + 16);
   p.work = reinterpret_cast<int2*>(sc + kScratchHeaderBytes);
   p.work_cap = static_cast<int>((plan->scratch_bytes - kScratchHeaderBytes) / 8);
-  const int64_t cap_items = plan->grid[0] / s.num_kv_heads;
   if (p.work_cap > cap_items) p.work_cap = static_cast<int>(cap_items);
 
   cudaError_t e;
-  cudaStream_t strm = static_cast<cudaStream_t>(stream);
-  switch (s.head_dim * 2 + (fp8 ? 1 : 0)) {
+  switch (s.head_dim * 2 + (fp8_tiles ? 1 : 0)) {
     case 128: e = launch_ext<64, 64, 4, 2, false>(tmq, tmk, tmv, p, strm); break;
     case 129: e = launch_ext<64, 64, 4, 2, true>(tmq, tmk, tmv, p, strm); break;
     case 256: e = launch_ext<128, 64, 2, 2, false>(tmq, tmk, tmv, p, strm); break;

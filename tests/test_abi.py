@@ -200,6 +200,20 @@ def test_plan_verify_scratch_scales_with_q_len(lib):
     assert four.launches == 2
 
 
+def test_plan_extend_e4m3_copy_choice(lib):
+    # an e4m3 extend plan dequantises into a bf16 copy while that copy
+    # (max_batch x max_pages_per_seq pages, K and V) fits in 2 GiB
+    kw = dict(mode=pb.MODE_EXTEND, kv_dtype=pb.KV_FP8_E4M3, max_batch=8, max_total_q=4096)
+    small = _plan(max_pages_per_seq=384, **kw)
+    copy_bytes = 8 * 384 * 16 * 8 * 128 * 2 * 2
+    assert small.kv_copy == 1 and small.launches == 3
+    bf16 = _plan(mode=pb.MODE_EXTEND, max_batch=8, max_total_q=4096, max_pages_per_seq=384)
+    assert bf16.kv_copy == 0 and bf16.launches == 2
+    assert small.scratch_bytes >= bf16.scratch_bytes + copy_bytes + 8 * 384 * 4
+    big = _plan(max_pages_per_seq=1 << 16, **kw)
+    assert big.kv_copy == 0 and big.launches == 2 and big.scratch_bytes < (1 << 20)
+
+
 def test_plan_single_split_makes_one_launch(lib):
     # one split per request: the split kernel writes the outputs, no merge launch
     one = _plan(num_splits=1)
