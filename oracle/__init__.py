@@ -69,6 +69,8 @@ class _Problem(ctypes.Structure):
         ("sinks", ctypes.c_void_p),
         ("k_scale", ctypes.c_float),
         ("v_scale", ctypes.c_float),
+        ("k_scales", ctypes.c_void_p),
+        ("v_scales", ctypes.c_void_p),
         ("rows", ctypes.c_void_p),
         ("num_rows", ctypes.c_int),
         ("out", ctypes.c_void_p),
@@ -145,8 +147,10 @@ def attention(p, rows=None, num_threads: int | None = None):
     ``p`` carries numpy arrays: q (uint16 bf16 bits [T, Hq, D]), k_cache /
     v_cache ([pages, page_size, Hkv, D], uint16 bf16 bits or uint8 e4m3
     codes, any strides), block_table, seq_lens, query_start_loc (extend) and
-    the scalar options.  ``rows`` optionally selects query rows.  Returns
-    (out [n, Hq, D] float64, lse [n, Hq] float64).
+    the scalar options; optional ``k_scales`` / ``v_scales`` ([batch] fp32)
+    are per-request e4m3 descales that replace ``k_scale`` / ``v_scale``.
+    ``rows`` optionally selects query rows.  Returns (out [n, Hq, D] float64,
+    lse [n, Hq] float64).
     """
     L = lib()
     q = p.q
@@ -161,6 +165,12 @@ def attention(p, rows=None, num_threads: int | None = None):
     qsl = None if p.query_start_loc is None else np.ascontiguousarray(p.query_start_loc, dtype=np.int32)
     sinks = None if p.sinks is None else np.ascontiguousarray(p.sinks, dtype=np.float32)
     B = int(sl.shape[0])
+    kss = getattr(p, "k_scales", None)
+    vss = getattr(p, "v_scales", None)
+    kss = None if kss is None else np.ascontiguousarray(kss, dtype=np.float32)
+    vss = None if vss is None else np.ascontiguousarray(vss, dtype=np.float32)
+    assert kss is None or kss.shape == (B,)
+    assert vss is None or vss.shape == (B,)
     T = q.shape[0]
     r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
     n = T if r is None else int(r.shape[0])
@@ -181,6 +191,7 @@ def attention(p, rows=None, num_threads: int | None = None):
         scale=float(p.scale), window=int(p.window), soft_cap=float(p.soft_cap),
         sinks=None if sinks is None else sinks.ctypes.data,
         k_scale=float(p.k_scale), v_scale=float(p.v_scale),
+        k_scales=None if kss is None else kss.ctypes.data, v_scales=None if vss is None else vss.ctypes.data,
         rows=None if r is None else r.ctypes.data, num_rows=n,
         out=out.ctypes.data, lse=lse.ctypes.data,
         num_threads=int(num_threads or os.cpu_count() or 1),

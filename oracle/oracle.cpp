@@ -192,6 +192,11 @@ typedef struct {
   const float* sinks;  // [num_q_heads] or NULL
   float k_scale;
   float v_scale;
+  // Per-request descales (the b12x backend's fp8 descale tensors, a scalar
+  // expanded to [num_reqs] or given per request): [batch] each, or NULL for
+  // the per-tensor k_scale / v_scale above.
+  const float* k_scales;
+  const float* v_scales;
   const int32_t* rows; // subset of query rows to evaluate, or NULL = all
   int num_rows;        // length of rows (ignored when rows == NULL)
   double* out;         // [n_rows_evaluated, num_q_heads, head_dim]
@@ -277,6 +282,9 @@ int oracle_attention(const oracle_problem* P) {
     const int pos_q = row_pos[k];
     const int r = row_idx[k];
     const int kvh = h / G;  // GQA head map ([TDA] cur_head // kv_group_num)
+    // fp8 descales of this request (per request when given, else per tensor)
+    const float k_sc = P->k_scales ? P->k_scales[b] : P->k_scale;
+    const float v_sc = P->v_scales ? P->v_scales[b] : P->v_scale;
     const uint16_t* qrow = P->q + static_cast<int64_t>(r) * P->q_stride_row +
                            static_cast<int64_t>(h) * P->q_stride_head;
 
@@ -298,9 +306,9 @@ int oracle_attention(const oracle_problem* P) {
       const int slot = j % ps;
       double dot = 0.0;
       for (int d = 0; d < D; ++d) {
-        const double kd = load_kv(P->k_cache, page, slot, kvh, d, P->k_scale);
+        const double kd = load_kv(P->k_cache, page, slot, kvh, d, k_sc);
         dot += bf16_bits_to_double(qrow[d]) * kd;
-        V[t * D + d] = load_kv(P->v_cache, page, slot, kvh, d, P->v_scale);
+        V[t * D + d] = load_kv(P->v_cache, page, slot, kvh, d, v_sc);
       }
       double sj = P->scale * dot;  // [TDA] qk *= sm_scale
       if (P->soft_cap > 0.0) {

@@ -54,6 +54,8 @@ class Problem:
     sinks: np.ndarray | None = None     # float32 [Hq]
     k_scale: float = 1.0
     v_scale: float = 1.0
+    k_scales: np.ndarray | None = None    # float32 [B]: per-request e4m3 descales (replace k_scale)
+    v_scales: np.ndarray | None = None
     kv_storage: np.ndarray | None = None  # backing array when K/V are views
     logical_k: list | None = field(default=None, repr=False)  # per request [L_b, Hkv, D]
     logical_v: list | None = field(default=None, repr=False)
@@ -94,6 +96,7 @@ def build_problem(mode: str, *, num_q_heads: int, num_kv_heads: int, head_dim: i
                   page_size: int, seq_lens, query_lens=None, kv_dtype: str = "bf16",
                   scale: float | None = None, window: int = 0, soft_cap: float = 0.0,
                   sinks: bool = False, k_scale: float = 1.0, v_scale: float = 1.0,
+                  k_scales=None, v_scales=None,
                   pool_extra: float = 0.10, pool_pages: int | None = None,
                   bt_width: int | None = None, seed: int = 0, layout: str = "separate",
                   poison: bool = True, keep_logical: bool = False, threads: int | None = None,
@@ -104,6 +107,8 @@ def build_problem(mode: str, *, num_q_heads: int, num_kv_heads: int, head_dim: i
     plus the new tokens, which are already in the pages).  ``query_lens``
     (extend only) gives the new tokens per request.  ``q_values`` (optional,
     float32 [T, Hq, D]) replaces the random queries; it is rounded to bf16.
+    ``k_scales`` / ``v_scales`` (e4m3 only, [B]) quantise each request's keys /
+    values with its own scale and are kept as per-request descales.
     """
     assert mode in ("decode", "extend")
     assert kv_dtype in ("bf16", "fp8_e4m3")
@@ -140,6 +145,11 @@ def build_problem(mode: str, *, num_q_heads: int, num_kv_heads: int, head_dim: i
 
     # KV storage, poisoned.
     fp8 = kv_dtype == "fp8_e4m3"
+    kss = None if k_scales is None else np.asarray(k_scales, np.float32).reshape(-1)
+    vss = None if v_scales is None else np.asarray(v_scales, np.float32).reshape(-1)
+    assert (kss is None and vss is None) or fp8, "per-request scales apply to an e4m3 cache"
+    assert kss is None or kss.shape == (B,)
+    assert vss is None or vss.shape == (B,)
     dt = np.uint8 if fp8 else np.uint16
     fill = (E4M3_NAN if fp8 else BF16_NAN) if poison else 0
     if layout == "separate":
@@ -176,7 +186,9 @@ def build_problem(mode: str, *, num_q_heads: int, num_kv_heads: int, head_dim: i
         kx = g.standard_normal((n, Hkv, D), dtype=np.float32)
         vx = g.standard_normal((n, Hkv, D), dtype=np.float32)
         if fp8:
-            kq, vq = _to_e4m3_codes(kx, k_scale), _to_e4m3_codes(vx, v_scale)
+            ksc = k_scale if kss is None else float(kss[b])
+            vsc = v_scale if vss is None else float(vss[b])
+            kq, vq = _to_e4m3_codes(kx, ksc), _to_e4m3_codes(vx, vsc)
         else:
             kq, vq = _to_bf16_bits(kx), _to_bf16_bits(vx)
         tok = np.arange(t0, L)
@@ -215,7 +227,7 @@ def build_problem(mode: str, *, num_q_heads: int, num_kv_heads: int, head_dim: i
         seq_lens=sl.astype(np.int32),
         query_start_loc=None if qsl is None else qsl.astype(np.int32),
         scale=float(scale), window=int(window), soft_cap=float(soft_cap), sinks=sk,
-        k_scale=float(k_scale), v_scale=float(v_scale), kv_storage=storage,
+        k_scale=float(k_scale), v_scale=float(v_scale), k_scales=kss, v_scales=vss, kv_storage=storage,
         logical_k=logical_k, logical_v=logical_v, name=name)
 
 

@@ -25,7 +25,9 @@ def e4m3_dequant_f64(codes: np.ndarray, scale: float) -> torch.Tensor:
 
 def logical_kv_f64(p, b):
     if p.kv_dtype == "fp8_e4m3":
-        return e4m3_dequant_f64(p.logical_k[b], p.k_scale), e4m3_dequant_f64(p.logical_v[b], p.v_scale)
+        ks = p.k_scale if p.k_scales is None else float(p.k_scales[b])
+        vs = p.v_scale if p.v_scales is None else float(p.v_scales[b])
+        return e4m3_dequant_f64(p.logical_k[b], ks), e4m3_dequant_f64(p.logical_v[b], vs)
     return bf16_bits_to_f64(p.logical_k[b]), bf16_bits_to_f64(p.logical_v[b])
 
 

@@ -111,6 +111,51 @@ def test_oracle_matches_sdpa(oracle_lib, mode, G, Hkv, D, ps, layout, kv):
         np.testing.assert_allclose(lse[rows], LSE.numpy(), rtol=0, atol=1e-11)
 
 
+@pytest.mark.parametrize("mode", ["decode", "extend"])
+def test_oracle_per_request_scales_match_sdpa(oracle_lib, mode):
+    # per-request e4m3 descales (the b12x backend's [num_reqs] descale
+    # tensors): each request's logical K/V dequantised with its own scales
+    ks, vs = [0.05, 0.11, 0.02], [0.07, 0.013, 0.3]
+    p = _problem(mode, seed=811, Hq=8, Hkv=2, D=16, ps=4, kv_dtype="fp8_e4m3", k_scales=ks, v_scales=vs)
+    out, lse = oracle.attention(p)
+    q = refs.bf16_bits_to_f64(p.q)
+    for b in range(p.batch):
+        rows = _rows_of(p, b)
+        k, v = refs.logical_kv_f64(p, b)
+        keep = refs.lower_right_causal(len(rows), int(p.seq_lens[b]))
+        O, LSE = refs.sdpa_with_lse(q[rows], k, v, keep, p.scale)
+        np.testing.assert_allclose(out[rows], O.numpy(), rtol=0, atol=1e-11)
+        np.testing.assert_allclose(lse[rows], LSE.numpy(), rtol=0, atol=1e-11)
+
+
+def test_per_request_scales_equal_to_scalar(oracle_lib):
+    # the same scale for every request is the per-tensor case, bit for bit
+    a = _problem("extend", seed=812, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.07)
+    b = _problem("extend", seed=812, kv_dtype="fp8_e4m3", k_scales=[0.05] * 3, v_scales=[0.07] * 3)
+    assert np.array_equal(a.k_cache, b.k_cache) and np.array_equal(a.v_cache, b.v_cache)
+    oa, la = oracle.attention(a)
+    ob, lb = oracle.attention(b)
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+
+
+def test_per_request_scales_follow_the_request(oracle_lib):
+    # each request of a mixed batch equals that request alone with its own
+    # scalar scales, over the same pages (a scale taken from the wrong request
+    # or row fails here)
+    import dataclasses
+    ks, vs = [0.05, 0.11, 0.02], [0.07, 0.013, 0.3]
+    p = _problem("extend", seed=813, kv_dtype="fp8_e4m3", k_scales=ks, v_scales=vs)
+    out, lse = oracle.attention(p)
+    qsl = p.query_start_loc
+    for b in range(p.batch):
+        r0, r1 = int(qsl[b]), int(qsl[b + 1])
+        one = dataclasses.replace(p, q=p.q[r0:r1], block_table=p.block_table[b:b + 1],
+                                  seq_lens=p.seq_lens[b:b + 1], query_start_loc=np.array([0, r1 - r0], np.int32),
+                                  k_scales=None, v_scales=None, k_scale=ks[b], v_scale=vs[b])
+        o1, l1 = oracle.attention(one)
+        assert np.array_equal(o1, out[r0:r1]) and np.array_equal(l1, lse[r0:r1]), b
+
+
 # ---- closed forms -----------------------------------------------------------
 
 def test_single_key_is_value_row(oracle_lib):
