@@ -133,6 +133,12 @@ pa_status pa_plan(const pa_shape* shape, const int32_t* host_seq_lens, int32_t b
  *   scale        softmax scale applied to q.K before the soft-cap
  *   sinks        device fp32 [Hq] when plan->shape.has_sinks, else NULL
  *   k_scale, v_scale  per-tensor fp8 scales (ignored for bf16 KV)
+ *   k_scales, v_scales  device fp32 [batch] per-request fp8 descales, or NULL;
+ *                each one given replaces its per-tensor scale (request b's
+ *                pages dequantise as bf16(float(code) * k_scales[b])), as the
+ *                b12x backend page's descales may be one value per request
+ *                ("vllm/v1/attention/backends/b12x", _prepare_fp8_descales);
+ *                ignored for bf16 KV
  *   out          device bf16 [batch, Hq, D], strides out_stride_tok / out_stride_head
  *   lse          device fp32 [batch, Hq] contiguous, or NULL
  *   scratch      device, >= plan->scratch_bytes bytes, 256-byte aligned; its
@@ -147,6 +153,7 @@ pa_status pa_decode(const pa_plan_t* plan,
                     const int32_t* block_table, int64_t bt_stride,
                     const int32_t* seq_lens, int32_t batch,
                     float scale, const float* sinks, float k_scale, float v_scale,
+                    const float* k_scales, const float* v_scales,
                     void* out, int64_t out_stride_tok, int64_t out_stride_head,
                     float* lse,
                     void* scratch, int64_t scratch_bytes, void* stream);
@@ -205,6 +212,7 @@ pa_status pa_extend(const pa_plan_t* plan,
                     const int32_t* seq_lens, const int32_t* query_start_loc,
                     int32_t batch, int32_t total_q,
                     float scale, const float* sinks, float k_scale, float v_scale,
+                    const float* k_scales, const float* v_scales,
                     void* out, int64_t out_stride_tok, int64_t out_stride_head,
                     float* lse,
                     void* scratch, int64_t scratch_bytes, void* stream);

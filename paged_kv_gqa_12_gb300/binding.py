@@ -92,10 +92,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.pa_plan.argtypes = [ctypes.POINTER(PaShape), vp, i32, ctypes.POINTER(PaPlan)]
     L.pa_plan.restype = ctypes.c_int
     L.pa_decode.argtypes = [ctypes.POINTER(PaPlan), vp, i64, i64, vp, vp, i64, i64, i64, i32, vp, i64,
-                            vp, i32, f32, vp, f32, f32, vp, i64, i64, vp, vp, i64, vp]
+                            vp, i32, f32, vp, f32, f32, vp, vp, vp, i64, i64, vp, vp, i64, vp]
     L.pa_decode.restype = ctypes.c_int
     L.pa_extend.argtypes = [ctypes.POINTER(PaPlan), vp, i64, i64, vp, vp, i64, i64, i64, i32, vp, i64,
-                            vp, vp, i32, i32, f32, vp, f32, f32, vp, i64, i64, vp, vp, i64, vp]
+                            vp, vp, i32, i32, f32, vp, f32, f32, vp, vp, vp, i64, i64, vp, vp, i64, vp]
     L.pa_extend.restype = ctypes.c_int
     L.pa_decode_static_scratch.argtypes = [ctypes.POINTER(PaPlan), vp, i64, i64, vp, vp, i64, i64, i64, i32,
                                            vp, i64, vp, i32, f32, vp, f32, f32, vp, i64, i64, vp, vp]
@@ -163,27 +163,32 @@ def _kv_strides(k_cache, v_cache):
 
 
 def decode(p: PaPlan, q, k_cache, v_cache, block_table, seq_lens, *, scale: float, out, lse=None,
-           sinks=None, k_scale: float = 1.0, v_scale: float = 1.0, scratch, stream=None):
-    """pa_decode on torch tensors (q/out [B, Hq, D] bf16; caches bf16 or uint8 e4m3)."""
+           sinks=None, k_scale: float = 1.0, v_scale: float = 1.0, k_scales=None, v_scales=None, scratch,
+           stream=None):
+    """pa_decode on torch tensors (q/out [B, Hq, D] bf16; caches bf16 or uint8 e4m3;
+    k_scales / v_scales: optional device fp32 [B] per-request descales)."""
     sp, st, sh = _kv_strides(k_cache, v_cache)
     status = load().pa_decode(
         ctypes.byref(p), _ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), sp, st, sh,
         k_cache.shape[0], _ptr(block_table), block_table.stride(0), _ptr(seq_lens), seq_lens.shape[0],
-        float(scale), _ptr(sinks), float(k_scale), float(v_scale), _ptr(out), out.stride(0), out.stride(1),
-        _ptr(lse), _ptr(scratch), scratch.numel() * scratch.element_size(), _stream(stream))
+        float(scale), _ptr(sinks), float(k_scale), float(v_scale), _ptr(k_scales), _ptr(v_scales), _ptr(out),
+        out.stride(0), out.stride(1), _ptr(lse), _ptr(scratch), scratch.numel() * scratch.element_size(),
+        _stream(stream))
     _check(status, "pa_decode")
 
 
 def extend(p: PaPlan, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, *, scale: float, out,
-           lse=None, sinks=None, k_scale: float = 1.0, v_scale: float = 1.0, scratch, stream=None):
-    """pa_extend on torch tensors (q/out [T, Hq, D] bf16)."""
+           lse=None, sinks=None, k_scale: float = 1.0, v_scale: float = 1.0, k_scales=None, v_scales=None,
+           scratch, stream=None):
+    """pa_extend on torch tensors (q/out [T, Hq, D] bf16; k_scales / v_scales:
+    optional device fp32 [B] per-request descales)."""
     sp, st, sh = _kv_strides(k_cache, v_cache)
     status = load().pa_extend(
         ctypes.byref(p), _ptr(q), q.stride(0), q.stride(1), _ptr(k_cache), _ptr(v_cache), sp, st, sh,
         k_cache.shape[0], _ptr(block_table), block_table.stride(0), _ptr(seq_lens), _ptr(query_start_loc),
-        seq_lens.shape[0], q.shape[0], float(scale), _ptr(sinks), float(k_scale), float(v_scale), _ptr(out),
-        out.stride(0), out.stride(1), _ptr(lse), _ptr(scratch), scratch.numel() * scratch.element_size(),
-        _stream(stream))
+        seq_lens.shape[0], q.shape[0], float(scale), _ptr(sinks), float(k_scale), float(v_scale), _ptr(k_scales),
+        _ptr(v_scales), _ptr(out), out.stride(0), out.stride(1), _ptr(lse), _ptr(scratch),
+        scratch.numel() * scratch.element_size(), _stream(stream))
     _check(status, "pa_extend")
 
 

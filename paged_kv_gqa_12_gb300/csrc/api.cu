@@ -222,7 +222,7 @@ using namespace pa;
 
 extern "C" {
 
-int32_t pa_version(void) { return 101; }
+int32_t pa_version(void) { return 102; }
 
 const char* pa_status_string(pa_status status) {
   switch (status) {
@@ -269,12 +269,14 @@ pa_status pa_decode(const pa_plan_t* plan, const void* q, int64_t q_stride_tok, 
                     const void* k_cache, const void* v_cache, int64_t kv_stride_page, int64_t kv_stride_tok,
                     int64_t kv_stride_head, int32_t num_pages, const int32_t* block_table, int64_t bt_stride,
                     const int32_t* seq_lens, int32_t batch, float scale, const float* sinks, float k_scale,
-                    float v_scale, void* out, int64_t out_stride_tok, int64_t out_stride_head, float* lse,
-                    void* scratch, int64_t scratch_bytes, void* stream) {
+                    float v_scale, const float* k_scales, const float* v_scales, void* out,
+                    int64_t out_stride_tok, int64_t out_stride_head, float* lse, void* scratch,
+                    int64_t scratch_bytes, void* stream) {
   if (!plan || plan->shape.mode != PA_MODE_DECODE) return PA_ERR_INVALID_ARG;
   return run_split_kv(plan, q, q_stride_tok, q_stride_head, k_cache, v_cache, kv_stride_page, kv_stride_tok,
                       kv_stride_head, num_pages, block_table, bt_stride, seq_lens, nullptr, batch, scale, sinks,
-                      k_scale, v_scale, out, out_stride_tok, out_stride_head, lse, scratch, scratch_bytes, stream);
+                      k_scale, v_scale, k_scales, v_scales, out, out_stride_tok, out_stride_head, lse, scratch,
+                      scratch_bytes, stream);
 }
 
 }  // extern "C"
@@ -285,8 +287,9 @@ pa_status run_split_kv(const pa_plan_t* plan, const void* q, int64_t q_stride_to
                        const void* k_cache, const void* v_cache, int64_t kv_stride_page, int64_t kv_stride_tok,
                        int64_t kv_stride_head, int32_t num_pages, const int32_t* block_table, int64_t bt_stride,
                        const int32_t* seq_lens, const int32_t* qsl, int32_t batch, float scale, const float* sinks,
-                       float k_scale, float v_scale, void* out, int64_t out_stride_tok, int64_t out_stride_head,
-                       float* lse, void* scratch, int64_t scratch_bytes, void* stream) {
+                       float k_scale, float v_scale, const float* k_scales, const float* v_scales, void* out,
+                       int64_t out_stride_tok, int64_t out_stride_head, float* lse, void* scratch,
+                       int64_t scratch_bytes, void* stream) {
   if (!plan) return PA_ERR_INVALID_ARG;
   const pa_shape& s = plan->shape;
   if ((s.mode != PA_MODE_DECODE && s.mode != PA_MODE_VERIFY) || validate_shape(s) != PA_OK) return PA_ERR_INVALID_ARG;
@@ -339,6 +342,8 @@ pa_status run_split_kv(const pa_plan_t* plan, const void* q, int64_t q_stride_to
   p.sinks = sinks;
   p.k_scale = fp8 ? k_scale : 1.f;
   p.v_scale = fp8 ? v_scale : 1.f;
+  p.k_scales = fp8 ? k_scales : nullptr;
+  p.v_scales = fp8 ? v_scales : nullptr;
   p.out = static_cast<uint16_t*>(out);
   p.out_stride_tok = out_stride_tok;
   p.out_stride_head = out_stride_head;

@@ -268,6 +268,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
   __syncwarp();
 
   const bool capped = p.cap_log2 > 0.f;
+  // e4m3 descales of this request (per request when given, else per tensor)
+  const float k_sc = p.k_scales != nullptr ? p.k_scales[b] : p.k_scale;
+  const float v_sc = p.v_scales != nullptr ? p.v_scales[b] : p.v_scale;
   int it = 0;
   for (int k = warp; k < n_tiles; k += kWarps, ++it) {
     const int stage = it % NS;
@@ -312,10 +315,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
 #pragma unroll
         for (int ks = 0; ks < T::KS; ++ks) {
           uint32_t a[4];
-          a[0] = dequant_e4m3x2(w0[ks], p.k_scale);
-          a[1] = dequant_e4m3x2(w1[ks], p.k_scale);
-          a[2] = dequant_e4m3x2(w0[ks] >> 16, p.k_scale);
-          a[3] = dequant_e4m3x2(w1[ks] >> 16, p.k_scale);
+          a[0] = dequant_e4m3x2(w0[ks], k_sc);
+          a[1] = dequant_e4m3x2(w1[ks], k_sc);
+          a[2] = dequant_e4m3x2(w0[ks] >> 16, k_sc);
+          a[3] = dequant_e4m3x2(w1[ks] >> 16, k_sc);
 #pragma unroll
           for (int j = 0; j < NH8; ++j) mma_bf16(s[mt][j], a, qf[ks][j][0], qf[ks][j][1]);
         }
@@ -449,10 +452,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
           const uint32_t x = __byte_perm(ra[i >> 1], rb[i >> 1], sel);
           const uint32_t y = __byte_perm(rc[i >> 1], rd[i >> 1], sel);
           uint32_t a[4];
-          a[0] = dequant_e4m3x2(x, p.v_scale) & vm_lo;
-          a[1] = dequant_e4m3x2(x >> 16, p.v_scale) & vm_lo;
-          a[2] = dequant_e4m3x2(y, p.v_scale) & vm_hi;
-          a[3] = dequant_e4m3x2(y >> 16, p.v_scale) & vm_hi;
+          a[0] = dequant_e4m3x2(x, v_sc) & vm_lo;
+          a[1] = dequant_e4m3x2(x >> 16, v_sc) & vm_lo;
+          a[2] = dequant_e4m3x2(y, v_sc) & vm_hi;
+          a[3] = dequant_e4m3x2(y >> 16, v_sc) & vm_hi;
 #pragma unroll
           for (int j = 0; j < NH8; ++j) {
             mma_bf16(o[i][j], a, pb[j][0], pb[j][1]);

@@ -66,5 +66,6 @@ extern "C" pa_status pa_decode_static_scratch(
     return PA_ERR_CUDA;
   return pa_decode(plan, q, q_stride_tok, q_stride_head, k_cache, v_cache, kv_stride_page, kv_stride_tok,
                    kv_stride_head, num_pages, block_table, bt_stride, seq_lens, batch, scale, sinks, k_scale,
-                   v_scale, out, out_stride_tok, out_stride_head, lse, scratch, pa::kStaticScratchBytes, stream);
+                   v_scale, nullptr, nullptr, out, out_stride_tok, out_stride_head, lse, scratch,
+                   pa::kStaticScratchBytes, stream);
 }

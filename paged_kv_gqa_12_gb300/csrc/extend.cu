@@ -67,6 +67,8 @@ struct ExtendParams {
   int window;
   const float* sinks;
   float k_scale, v_scale;   // fp8 cache: per-tensor dequantisation scales
+  const float* k_scales;    // fp8 cache: [B] per-request scales replacing them, or null
+  const float* v_scales;
   uint16_t* out;
   int64_t out_stride_tok, out_stride_head;
   float* lse;
@@ -405,7 +407,8 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       // e4m3 tiles land in the stage (NST ahead), then this warp dequantises
       // them in place and marks the stage full
       uint64_t* land = is_k ? k_land : v_land;
-      const float scale = is_k ? p.k_scale : p.v_scale;
+      const float* per_req = is_k ? p.k_scales : p.v_scales;
+      const float scale = per_req != nullptr ? per_req[b] : (is_k ? p.k_scale : p.v_scale);
       auto fetch = [&](int j) {
         const int stage = j % NST;
         if (lane == 0) mbar_arrive_expect_tx(&land[stage], static_cast<uint32_t>(BN * D));
@@ -733,6 +736,8 @@ struct KvCopyParams {
   const int32_t* qsl;
   int batch, num_pages, page_size, num_kv_heads, window, maxp, max_kv;
   float k_scale, v_scale;
+  const float* k_scales;   // [B] per-request scales, or null
+  const float* v_scales;
   uint16_t* kc;
   uint16_t* vc;
   int32_t* bt_copy;
@@ -753,6 +758,8 @@ __global__ void __launch_bounds__(256) extend_kv_copy_kernel(const KvCopyParams 
   const int first = p.window > 0 ? max(0, ctx - p.window + 1) : 0;   // first key any query attends
   if ((i + 1) * ps <= first || i * ps >= L) return;
   const int src = p.block_table[static_cast<int64_t>(b) * p.bt_stride + i];
+  const float k_sc = p.k_scales != nullptr ? p.k_scales[b] : p.k_scale;
+  const float v_sc = p.v_scales != nullptr ? p.v_scales[b] : p.v_scale;
   constexpr int UPH = D / 16;   // 16-code units per head row
   const int units = ps * p.num_kv_heads * UPH;
   const int64_t page_elems = static_cast<int64_t>(ps) * p.num_kv_heads * D;
@@ -780,10 +787,10 @@ __global__ void __launch_bounds__(256) extend_kv_copy_kernel(const KvCopyParams 
     uint32_t ko[8], vo[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      ko[2 * k] = dequant_e4m3x2(ka[k] & 0xffffu, p.k_scale);
-      ko[2 * k + 1] = dequant_e4m3x2(ka[k] >> 16, p.k_scale);
-      vo[2 * k] = dequant_e4m3x2(va[k] & 0xffffu, p.v_scale);
-      vo[2 * k + 1] = dequant_e4m3x2(va[k] >> 16, p.v_scale);
+      ko[2 * k] = dequant_e4m3x2(ka[k] & 0xffffu, k_sc);
+      ko[2 * k + 1] = dequant_e4m3x2(ka[k] >> 16, k_sc);
+      vo[2 * k] = dequant_e4m3x2(va[k] & 0xffffu, v_sc);
+      vo[2 * k + 1] = dequant_e4m3x2(va[k] >> 16, v_sc);
     }
     kd[2 * u] = make_uint4(ko[0], ko[1], ko[2], ko[3]);
     kd[2 * u + 1] = make_uint4(ko[4], ko[5], ko[6], ko[7]);
@@ -864,9 +871,9 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
                                int64_t kv_stride_tok, int64_t kv_stride_head, int32_t num_pages,
                                const int32_t* block_table, int64_t bt_stride, const int32_t* seq_lens,
                                const int32_t* query_start_loc, int32_t batch, int32_t total_q, float scale,
-                               const float* sinks, float k_scale, float v_scale, void* out, int64_t out_stride_tok,
-                               int64_t out_stride_head, float* lse, void* scratch, int64_t scratch_bytes,
-                               void* stream) {
+                               const float* sinks, float k_scale, float v_scale, const float* k_scales,
+                               const float* v_scales, void* out, int64_t out_stride_tok, int64_t out_stride_head,
+                               float* lse, void* scratch, int64_t scratch_bytes, void* stream) {
   if (!plan) return PA_ERR_INVALID_ARG;
   const pa_shape& s = plan->shape;
   if (s.mode == PA_MODE_VERIFY) {
@@ -876,8 +883,8 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
     if (!query_start_loc && batch > 0) return PA_ERR_INVALID_ARG;
     return run_split_kv(plan, q, q_stride_tok, q_stride_head, k_cache, v_cache, kv_stride_page, kv_stride_tok,
                         kv_stride_head, num_pages, block_table, bt_stride, seq_lens, query_start_loc, batch, scale,
-                        sinks, k_scale, v_scale, out, out_stride_tok, out_stride_head, lse, scratch, scratch_bytes,
-                        stream);
+                        sinks, k_scale, v_scale, k_scales, v_scales, out, out_stride_tok, out_stride_head, lse,
+                        scratch, scratch_bytes, stream);
   }
   if (s.mode != PA_MODE_EXTEND || validate_shape(s) != PA_OK) return PA_ERR_INVALID_ARG;
   const bool fp8 = s.kv_dtype == PA_KV_FP8_E4M3;
@@ -944,6 +951,8 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
     cp.max_kv = s.max_pages_per_seq * s.page_size;
     cp.k_scale = k_scale;
     cp.v_scale = v_scale;
+    cp.k_scales = k_scales;
+    cp.v_scales = v_scales;
     cp.kc = reinterpret_cast<uint16_t*>(kc);
     cp.vc = reinterpret_cast<uint16_t*>(vc);
     cp.bt_copy = bt_copy;
@@ -993,6 +1002,8 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
   p.sinks = sinks;
   p.k_scale = fp8_tiles ? k_scale : 1.f;
   p.v_scale = fp8_tiles ? v_scale : 1.f;
+  p.k_scales = fp8_tiles ? k_scales : nullptr;
+  p.v_scales = fp8_tiles ? v_scales : nullptr;
   p.out = static_cast<uint16_t*>(out);
   p.out_stride_tok = out_stride_tok;
   p.out_stride_head = out_stride_head;

@@ -32,6 +32,8 @@ struct DecodeParams {
   int window;                 // 0 = off
   const float* sinks;         // [Hq] or null
   float k_scale, v_scale;
+  const float* k_scales;      // fp8: [B] per-request scales replacing k_scale, or null
+  const float* v_scales;
   uint16_t* out;              // bf16 [B, Hq, D]
   int64_t out_stride_tok, out_stride_head;
   float* lse;                 // [B, Hq] or null
@@ -73,8 +75,9 @@ pa_status run_split_kv(const pa_plan_t* plan, const void* q, int64_t q_stride_to
                        const void* k_cache, const void* v_cache, int64_t kv_stride_page, int64_t kv_stride_tok,
                        int64_t kv_stride_head, int32_t num_pages, const int32_t* block_table, int64_t bt_stride,
                        const int32_t* seq_lens, const int32_t* qsl, int32_t batch, float scale, const float* sinks,
-                       float k_scale, float v_scale, void* out, int64_t out_stride_tok, int64_t out_stride_head,
-                       float* lse, void* scratch, int64_t scratch_bytes, void* stream);
+                       float k_scale, float v_scale, const float* k_scales, const float* v_scales, void* out,
+                       int64_t out_stride_tok, int64_t out_stride_head, float* lse, void* scratch,
+                       int64_t scratch_bytes, void* stream);
 
 // Kernel-variant table shared by the planner and the launcher.
 DecodeConfig decode_config(int head_dim, bool fp8, int rows, int bt_cache);

@@ -33,6 +33,9 @@ def upload(p, device="cuda"):
     d["sl"] = torch.from_numpy(p.seq_lens).to(device)
     d["qsl"] = None if p.query_start_loc is None else torch.from_numpy(p.query_start_loc).to(device)
     d["sinks"] = None if p.sinks is None else torch.from_numpy(p.sinks).to(device)
+    ks, vs = getattr(p, "k_scales", None), getattr(p, "v_scales", None)
+    d["k_scales"] = None if ks is None else torch.from_numpy(np.ascontiguousarray(ks, np.float32)).to(device)
+    d["v_scales"] = None if vs is None else torch.from_numpy(np.ascontiguousarray(vs, np.float32)).to(device)
     return d
 
 
@@ -61,7 +64,7 @@ def run(p, d=None, plan=None, num_splits=0, host_lens=True, with_lse=True, verif
     lse = torch.full((T, Hq), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
     scratch = pb.alloc_scratch(plan)
     kw = dict(scale=p.scale, out=out, lse=lse, sinks=d["sinks"], k_scale=p.k_scale, v_scale=p.v_scale,
-              scratch=scratch)
+              k_scales=d.get("k_scales"), v_scales=d.get("v_scales"), scratch=scratch)
     if p.mode == "decode":
         pb.decode(plan, d["q"], d["k"], d["v"], d["bt"], d["sl"], **kw)
     else:

@@ -135,7 +135,7 @@ def _decode_args(plan, **over):
     vp = ctypes.c_void_p
     return L.pa_decode(ctypes.byref(a["plan"]), vp(a["q"]), a["qs"][0], a["qs"][1], vp(a["k"]), vp(a["v"]),
                        a["kvs"][0], a["kvs"][1], a["kvs"][2], a["pages"], vp(a["bt"]), a["bts"], vp(a["sl"]),
-                       a["batch"], a["scale"], vp(a["sinks"]) if a["sinks"] else None, a["ks"], a["vs"],
+                       a["batch"], a["scale"], vp(a["sinks"]) if a["sinks"] else None, a["ks"], a["vs"], None, None,
                        vp(a["out"]), a["os"][0], a["os"][1], vp(a["lse"]) if a["lse"] else None,
                        vp(a["scratch"]) if a["scratch"] else None, a["sbytes"], None)
 
