@@ -89,43 +89,6 @@ def test_plan_rejects(lib, bad, status):
     assert ei.value.status == status
 
 
-class _Fake:
-    """A stand-in tensor with a fixed fake address: only host-side checks
-    that fail before any CUDA call are exercised with it."""
-
-    def __init__(self, addr, shape=(4, 8, 128), strides=None, itemsize=2):
-        self._addr = addr
-        self.shape = shape
-        self._strides = strides or tuple(int(x) for x in _contig(shape))
-        self._itemsize = itemsize
-
-    def data_ptr(self):
-        return self._addr
-
-    def stride(self, i=None):
-        return self._strides if i is None else self._strides[i]
-
-    def dim(self):
-        return len(self.shape)
-
-    def numel(self):
-        n = 1
-        for s in self.shape:
-            n *= s
-        return n
-
-    def element_size(self):
-        return self._itemsize
-
-
-def _contig(shape):
-    st, acc = [], 1
-    for s in reversed(shape):
-        st.append(acc)
-        acc *= s
-    return list(reversed(st))
-
-
 def _decode_args(plan, **over):
     a = dict(plan=plan, q=0x10000, qs=(32 * 128, 128), k=0x20000, v=0x40000, kvs=(16 * 8 * 128, 8 * 128, 128),
              pages=100, bt=0x50000, bts=512, sl=0x60000, batch=4, scale=0.088, sinks=None, ks=1.0, vs=1.0,
