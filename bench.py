@@ -38,8 +38,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DECODE_CFG = 2
-EXTEND_CFG = 4
+DECODE_WORKLOAD = "decode_llama3_8b"
+EXTEND_WORKLOAD = "prefill"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -207,8 +207,8 @@ def run_ours(args):
                     sinks=None if p.sinks is None else t(p.sinks))
 
     # Weak scaling: each rank holds its own copy of the per-GPU workload.
-    dp = wl.config_problem(DECODE_CFG, batch=args.decode_batch)
-    ep = wl.config_problem(EXTEND_CFG, batch=args.extend_batch)
+    dp = wl.workload_problem(DECODE_WORKLOAD, batch=args.decode_batch)
+    ep = wl.workload_problem(EXTEND_WORKLOAD, batch=args.extend_batch)
     dd, ed = upload(dp), upload(ep)
     kvd = pb.KV_BF16
     dplan_kw = dict(mode=pb.MODE_DECODE, num_q_heads=dp.num_q_heads, num_kv_heads=dp.num_kv_heads,
@@ -370,7 +370,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; N(0,1) values, shuffled page pools)",
-        "config": {"workload": "decode " + wl.CONFIG_NAMES[DECODE_CFG] + " + extend " + wl.CONFIG_NAMES[EXTEND_CFG],
+        "config": {"workload": "decode " + wl.WORKLOADS[DECODE_WORKLOAD] + " + extend " + wl.WORKLOADS[EXTEND_WORKLOAD],
                    "decode_batch": dp.batch, "decode_tokens": int(dp.seq_lens.sum()),
                    "extend_batch": ep.batch, "extend_q_rows": ep.num_rows,
                    "l2": "not flushed: each step streams > 1.2 GB (L2 129 MB) in a fixed order",
@@ -438,7 +438,7 @@ def measure_extras(pb, wl, dp, dd, dev, stream):
                      "frac_of_hbm": round(vb / t / 1e9 / float(peaks.get("hbm_gbs", 6800.0)), 4),
                      "device_error": pb.check(vscr)}
     # extend with an e4m3 cache
-    ep8 = wl.config_problem(EXTEND_CFG, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05)
+    ep8 = wl.workload_problem(EXTEND_WORKLOAD, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05)
 
     def t8(a):
         if a.dtype == np.uint16:
@@ -493,7 +493,7 @@ def run_reference(args):
         return
     import oracle
     from paged_kv_gqa_12_gb300 import workloads as wl
-    p = wl.config_problem(DECODE_CFG)
+    p = wl.workload_problem(DECODE_WORKLOAD)
     cores = os.cpu_count() or 1
     K, W = args.steps, args.warmup
     # bounded per-step sample: one request (all heads) per step, cycling
@@ -512,7 +512,7 @@ def run_reference(args):
             "value": value, "unit": "TB/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": K,
             "warmup": W, "ms_per_step": tot / K * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": "decode " + wl.CONFIG_NAMES[DECODE_CFG]},
+            "config": {"workload": "decode " + wl.WORKLOADS[DECODE_WORKLOAD]},
             "cpu_baseline": {"value": value, "unit": "TB/s", "cores": cores, "kind": "oracle",
                              "sample": "one decode request (all heads) per step, cycling through the batch"},
             "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

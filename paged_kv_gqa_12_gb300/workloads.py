@@ -233,54 +233,56 @@ def build_problem(mode: str, *, num_q_heads: int, num_kv_heads: int, head_dim: i
 
 # ---- the five benchmark workloads --------------------------------------------
 
-CONFIG_NAMES = {
-    1: "decode-tiny B4 Hq8 Hkv2 D64 ps16 S4",
-    2: "decode Llama-3-8B-shaped B64 Hq32 Hkv8 D128 ps16 bf16 L~U[512,8192]",
-    3: "decode fp8-e4m3 B128 Hq64 Hkv8 D64 ps64 window1024 sinks L~logU[1024,32768]",
-    4: "extend B8 Hq32 Hkv8 D128 ps16 ctx~U[0,4096] q~U[1,2048]",
-    5: "decode softcap50 window4096 B256 Hq16 Hkv8 D256 ps32 L~lognormal(2048,1)",
+WORKLOADS = {
+    "decode_tiny": "decode-tiny B4 Hq8 Hkv2 D64 ps16 S4",
+    "decode_llama3_8b": "decode Llama-3-8B-shaped B64 Hq32 Hkv8 D128 ps16 bf16 L~U[512,8192]",
+    "decode_e4m3_window": "decode fp8-e4m3 B128 Hq64 Hkv8 D64 ps64 window1024 sinks L~logU[1024,32768]",
+    "prefill": "extend B8 Hq32 Hkv8 D128 ps16 ctx~U[0,4096] q~U[1,2048]",
+    "decode_softcap_d256": "decode softcap50 window4096 B256 Hq16 Hkv8 D256 ps32 L~lognormal(2048,1)",
 }
+# default seed of each workload's draws
+_SEEDS = {"decode_tiny": 1001, "decode_llama3_8b": 1002, "decode_e4m3_window": 1003, "prefill": 1004,
+          "decode_softcap_d256": 1005}
 
 
-def config_problem(cid: int, seed: int | None = None, batch: int | None = None, **kw) -> Problem:
-    """The five workloads: shapes, distributions and options as specified for
-    each benchmark configuration; seed defaults to 1000 + config id.
-    ``batch`` keeps only the first requests (same draws), for reduced cases."""
-    seed = 1000 + cid if seed is None else seed
+def workload_problem(name: str, seed: int | None = None, batch: int | None = None, **kw) -> Problem:
+    """One of the five benchmark workloads (``WORKLOADS``): shapes,
+    distributions and options as each is specified.  ``batch`` keeps only the
+    first requests (same draws), for reduced cases."""
+    if name not in WORKLOADS:
+        raise ValueError(f"unknown workload {name!r}")
+    seed = _SEEDS[name] if seed is None else seed
     rng = np.random.default_rng(seed + 7919)
-    name = CONFIG_NAMES[cid]
+    desc = WORKLOADS[name]
     cut = slice(None) if batch is None else slice(0, batch)
-    if cid == 1:
+    if name == "decode_tiny":
         B = 4
         sl = rng.integers(1, 301, size=B)[cut]
         args = dict(num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=16,
                     seq_lens=sl, scale=64 ** -0.5, pool_pages=128)
-        return build_problem("decode", seed=seed, name=name, **{**args, **kw})
-    if cid == 2:
+        return build_problem("decode", seed=seed, name=desc, **{**args, **kw})
+    if name == "decode_llama3_8b":
         B = 64
         sl = rng.integers(512, 8193, size=B)[cut]
         args = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
                     seq_lens=sl, scale=128 ** -0.5)
-        return build_problem("decode", seed=seed, name=name, **{**args, **kw})
-    if cid == 3:
+        return build_problem("decode", seed=seed, name=desc, **{**args, **kw})
+    if name == "decode_e4m3_window":
         B = 128
         sl = np.floor(np.exp(rng.uniform(math.log(1024), math.log(32768), size=B))).astype(np.int64)[cut]
         args = dict(num_q_heads=64, num_kv_heads=8, head_dim=64, page_size=64,
                     seq_lens=sl, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05,
                     window=1024, sinks=True, scale=64 ** -0.5)
-        return build_problem("decode", seed=seed, name=name, **{**args, **kw})
-    if cid == 4:
+        return build_problem("decode", seed=seed, name=desc, **{**args, **kw})
+    if name == "prefill":
         B = 8
         ctx = rng.integers(0, 4097, size=B)[cut]
         ql = rng.integers(1, 2049, size=B)[cut]
         args = dict(num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
                     seq_lens=ctx + ql, query_lens=ql, scale=128 ** -0.5)
-        return build_problem("extend", seed=seed, name=name, **{**args, **kw})
-    if cid == 5:
-        B = 256
-        sl = np.clip(np.rint(rng.lognormal(math.log(2048), 1.0, size=B)), 1, 65536).astype(np.int64)[cut]
-        args = dict(num_q_heads=16, num_kv_heads=8, head_dim=256, page_size=32,
-                    seq_lens=sl, soft_cap=50.0, window=4096, scale=256 ** -0.5)
-        return build_problem("decode", seed=seed, name=name, **{**args, **kw})
-    raise ValueError(f"unknown config {cid}")
-
+        return build_problem("extend", seed=seed, name=desc, **{**args, **kw})
+    B = 256   # decode_softcap_d256
+    sl = np.clip(np.rint(rng.lognormal(math.log(2048), 1.0, size=B)), 1, 65536).astype(np.int64)[cut]
+    args = dict(num_q_heads=16, num_kv_heads=8, head_dim=256, page_size=32,
+                seq_lens=sl, soft_cap=50.0, window=4096, scale=256 ** -0.5)
+    return build_problem("decode", seed=seed, name=desc, **{**args, **kw})

@@ -57,7 +57,7 @@ def test_decode_variants(Hq, Hkv, D, ps, kv, opts):
 
 
 def test_tiny_decode_split_counts():
-    p = wl.config_problem(1)
+    p = wl.workload_problem("decode_tiny")
     ref_o, ref_l = oracle.attention(p)
     for ns in (4, 1, 2, 3, 7, 0):
         out, lse = gh.run(p, num_splits=ns)
@@ -146,16 +146,16 @@ def test_no_lse_output():
     gh.assert_parity(out, None, ref_o, None)
 
 
-@pytest.mark.parametrize("cid", [2, 3, 5])
-def test_full_size_decode_workloads_sampled(cid):
+@pytest.mark.parametrize("name", ["decode_llama3_8b", "decode_e4m3_window", "decode_softcap_d256"])
+def test_full_size_decode_workloads_sampled(name):
     # The benchmark workloads at full size, in the launch configuration the
     # benchmark uses (planner with host lengths); the oracle evaluates a
     # sample of rows one by one.
-    p = wl.config_problem(cid)
+    p = wl.workload_problem(name)
     out, lse = gh.run(p)
-    rng = np.random.default_rng(cid)
+    rng = np.random.default_rng(len(name))
     rows = np.unique(np.concatenate([rng.choice(p.batch, size=12, replace=False),
                                      [int(np.argmax(p.seq_lens)), int(np.argmin(p.seq_lens))]])).astype(np.int32)
     ref_o, ref_l = oracle.attention(p, rows=rows)
-    gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what=wl.CONFIG_NAMES[cid])
+    gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what=wl.WORKLOADS[name])
     assert np.isfinite(out).all() and np.isfinite(lse).all()

@@ -101,7 +101,7 @@ def test_extend_empty_request_rows():
 
 
 def test_extend_full_size_workload_sampled():
-    p = wl.config_problem(4)
+    p = wl.workload_problem("prefill")
     out, lse = gh.run(p)
     assert np.isfinite(out).all() and np.isfinite(lse).all()
     rng = np.random.default_rng(4)
