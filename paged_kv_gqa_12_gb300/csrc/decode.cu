@@ -30,6 +30,7 @@
 //     otherwise the merge kernel combines the splits.
 #include <cfloat>
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -383,86 +384,108 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     }
 
     // ---- O^T += V^T P^T -----------------------------------------------------
+    // On tiles where some row masks a key (sequence start or end, window edge,
+    // a verify row's own position) P = P_hi + P_lo, both bf16: two MMAs make
+    // the weights exact to ~2^-17 (one bf16 P can be 2^-9 off, which a row
+    // with few attended keys does not average out), and masked keys' V rows
+    // are zeroed.  Every row of an unmasked tile attends to all its keys and
+    // to the tiles before it: one bf16 P, no masks.  Two compiled versions,
+    // chosen per tile.
+    auto pv = [&](auto exact_tag) {
+      constexpr bool EXACT = decltype(exact_tag)::value;
 #pragma unroll
-    for (int mt = 0; mt < T::MT; ++mt) {
-      // P = P_hi + P_lo, both bf16: two MMAs make the weights exact to ~2^-17
-      // (one bf16 P can be 2^-9 off, which a row with few attended keys does
-      // not average out); the tensor pipe has room, the kernel is HBM-bound.
-      uint32_t pb[NH8][2], pl[NH8][2];
+      for (int mt = 0; mt < T::MT; ++mt) {
+        uint32_t pb[NH8][2], pl[NH8][2];
 #pragma unroll
-      for (int j = 0; j < NH8; ++j) {
-        const uint32_t h0 = pack_bf16x2(s[mt][j][0], s[mt][j][1]);
-        const uint32_t h1 = pack_bf16x2(s[mt][j][2], s[mt][j][3]);
-        const uint32_t l0 = pack_bf16x2(s[mt][j][0] - __uint_as_float(h0 << 16),
-                                        s[mt][j][1] - __uint_as_float(h0 & 0xffff0000u));
-        const uint32_t l1 = pack_bf16x2(s[mt][j][2] - __uint_as_float(h1 << 16),
-                                        s[mt][j][3] - __uint_as_float(h1 & 0xffff0000u));
-        pb[j][0] = movmatrix_t(h0);
-        pb[j][1] = movmatrix_t(h1);
-        pl[j][0] = movmatrix_t(l0);
-        pl[j][1] = movmatrix_t(l1);
-      }
-      // Masked keys have P = 0, but their V rows may be stale or NaN: zero
-      // them in the fragment so 0 * NaN never reaches the accumulator.
-      uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-      if (partial) {
-        const int tk = t0 + mt * 16 + 2 * c;
-        auto valid = [&](int t) { return t >= tok_lo && t < tok_hi; };
-        vm_lo = (valid(tk) ? 0x0000ffffu : 0u) | (valid(tk + 1) ? 0xffff0000u : 0u);
-        vm_hi = (valid(tk + 8) ? 0x0000ffffu : 0u) | (valid(tk + 9) ? 0xffff0000u : 0u);
-      }
-      if constexpr (!FP8) {
-        const int mi = lane >> 3, rr = lane & 7;
-        const int tok = mt * 16 + rr + ((mi >> 1) << 3);
-#pragma unroll
-        for (int i = 0; i < T::KS; ++i) {
-          uint32_t a[4];
-          ldsm_x4_t(a, vst_u + T::off(tok, (i * 16 + ((mi & 1) << 3)) * 2));
-          a[0] &= vm_lo;
-          a[1] &= vm_lo;
-          a[2] &= vm_hi;
-          a[3] &= vm_hi;
-#pragma unroll
-          for (int j = 0; j < NH8; ++j) {
-            mma_bf16(o[i][j], a, pb[j][0], pb[j][1]);
-            mma_bf16(o[i][j], a, pl[j][0], pl[j][1]);
+        for (int j = 0; j < NH8; ++j) {
+          const uint32_t h0 = pack_bf16x2(s[mt][j][0], s[mt][j][1]);
+          const uint32_t h1 = pack_bf16x2(s[mt][j][2], s[mt][j][3]);
+          pb[j][0] = movmatrix_t(h0);
+          pb[j][1] = movmatrix_t(h1);
+          if constexpr (EXACT) {
+            const uint32_t l0 = pack_bf16x2(s[mt][j][0] - __uint_as_float(h0 << 16),
+                                            s[mt][j][1] - __uint_as_float(h0 & 0xffff0000u));
+            const uint32_t l1 = pack_bf16x2(s[mt][j][2] - __uint_as_float(h1 << 16),
+                                            s[mt][j][3] - __uint_as_float(h1 & 0xffff0000u));
+            pl[j][0] = movmatrix_t(l0);
+            pl[j][1] = movmatrix_t(l1);
           }
         }
-      } else {
-        // thread g owns output dims [g*D/8, (g+1)*D/8): m-tile i row g -> dim
-        // g*D/8 + 2i, row g+8 -> g*D/8 + 2i + 1.
-        constexpr int NW = D / 32;  // 32-bit words per thread per row
-        uint32_t ra[NW], rb[NW], rc[NW], rd[NW];
-        const int rowa = mt * 16 + 2 * c;
-#pragma unroll
-        for (int u = 0; u < NW; u += 2) {
-          const int byte = g * (D / 8) + 4 * u;
-          const uint2 xa = *reinterpret_cast<const uint2*>(vst + T::off(rowa, byte));
-          const uint2 xb = *reinterpret_cast<const uint2*>(vst + T::off(rowa + 1, byte));
-          const uint2 xc = *reinterpret_cast<const uint2*>(vst + T::off(rowa + 8, byte));
-          const uint2 xd = *reinterpret_cast<const uint2*>(vst + T::off(rowa + 9, byte));
-          ra[u] = xa.x; ra[u + 1] = xa.y;
-          rb[u] = xb.x; rb[u + 1] = xb.y;
-          rc[u] = xc.x; rc[u + 1] = xc.y;
-          rd[u] = xd.x; rd[u + 1] = xd.y;
+        // Masked keys have P = 0, but their V rows may be stale or NaN: zero
+        // them in the fragment so 0 * NaN never reaches the accumulator.
+        uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+        if constexpr (EXACT) {
+          const int tk = t0 + mt * 16 + 2 * c;
+          auto valid = [&](int t) { return t >= tok_lo && t < tok_hi; };
+          vm_lo = (valid(tk) ? 0x0000ffffu : 0u) | (valid(tk + 1) ? 0xffff0000u : 0u);
+          vm_hi = (valid(tk + 8) ? 0x0000ffffu : 0u) | (valid(tk + 9) ? 0xffff0000u : 0u);
         }
+        if constexpr (!FP8) {
+          const int mi = lane >> 3, rr = lane & 7;
+          const int tok = mt * 16 + rr + ((mi >> 1) << 3);
 #pragma unroll
-        for (int i = 0; i < T::KS; ++i) {
-          const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
-          const uint32_t x = __byte_perm(ra[i >> 1], rb[i >> 1], sel);
-          const uint32_t y = __byte_perm(rc[i >> 1], rd[i >> 1], sel);
-          uint32_t a[4];
-          a[0] = dequant_e4m3x2(x, v_sc) & vm_lo;
-          a[1] = dequant_e4m3x2(x >> 16, v_sc) & vm_lo;
-          a[2] = dequant_e4m3x2(y, v_sc) & vm_hi;
-          a[3] = dequant_e4m3x2(y >> 16, v_sc) & vm_hi;
+          for (int i = 0; i < T::KS; ++i) {
+            uint32_t a[4];
+            ldsm_x4_t(a, vst_u + T::off(tok, (i * 16 + ((mi & 1) << 3)) * 2));
+            if constexpr (EXACT) {
+              a[0] &= vm_lo;
+              a[1] &= vm_lo;
+              a[2] &= vm_hi;
+              a[3] &= vm_hi;
+            }
 #pragma unroll
-          for (int j = 0; j < NH8; ++j) {
-            mma_bf16(o[i][j], a, pb[j][0], pb[j][1]);
-            mma_bf16(o[i][j], a, pl[j][0], pl[j][1]);
+            for (int j = 0; j < NH8; ++j) {
+              mma_bf16(o[i][j], a, pb[j][0], pb[j][1]);
+              if constexpr (EXACT) mma_bf16(o[i][j], a, pl[j][0], pl[j][1]);
+            }
+          }
+        } else {
+          // thread g owns output dims [g*D/8, (g+1)*D/8): m-tile i row g -> dim
+          // g*D/8 + 2i, row g+8 -> g*D/8 + 2i + 1.
+          constexpr int NW = D / 32;  // 32-bit words per thread per row
+          uint32_t ra[NW], rb[NW], rc[NW], rd[NW];
+          const int rowa = mt * 16 + 2 * c;
+#pragma unroll
+          for (int u = 0; u < NW; u += 2) {
+            const int byte = g * (D / 8) + 4 * u;
+            const uint2 xa = *reinterpret_cast<const uint2*>(vst + T::off(rowa, byte));
+            const uint2 xb = *reinterpret_cast<const uint2*>(vst + T::off(rowa + 1, byte));
+            const uint2 xc = *reinterpret_cast<const uint2*>(vst + T::off(rowa + 8, byte));
+            const uint2 xd = *reinterpret_cast<const uint2*>(vst + T::off(rowa + 9, byte));
+            ra[u] = xa.x; ra[u + 1] = xa.y;
+            rb[u] = xb.x; rb[u + 1] = xb.y;
+            rc[u] = xc.x; rc[u + 1] = xc.y;
+            rd[u] = xd.x; rd[u + 1] = xd.y;
+          }
+#pragma unroll
+          for (int i = 0; i < T::KS; ++i) {
+            const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+            const uint32_t x = __byte_perm(ra[i >> 1], rb[i >> 1], sel);
+            const uint32_t y = __byte_perm(rc[i >> 1], rd[i >> 1], sel);
+            uint32_t a[4];
+            a[0] = dequant_e4m3x2(x, v_sc);
+            a[1] = dequant_e4m3x2(x >> 16, v_sc);
+            a[2] = dequant_e4m3x2(y, v_sc);
+            a[3] = dequant_e4m3x2(y >> 16, v_sc);
+            if constexpr (EXACT) {
+              a[0] &= vm_lo;
+              a[1] &= vm_lo;
+              a[2] &= vm_hi;
+              a[3] &= vm_hi;
+            }
+#pragma unroll
+            for (int j = 0; j < NH8; ++j) {
+              mma_bf16(o[i][j], a, pb[j][0], pb[j][1]);
+              if constexpr (EXACT) mma_bf16(o[i][j], a, pl[j][0], pl[j][1]);
+            }
           }
         }
       }
+    };
+    if (partial) {
+      pv(std::true_type{});
+    } else {
+      pv(std::false_type{});
     }
 
     __syncwarp();
