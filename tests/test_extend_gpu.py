@@ -156,3 +156,21 @@ def test_extend_fp8_copy_and_in_kernel_paths_agree():
         assert np.array_equal(o1, o2) and np.array_equal(l1, l2), opts
         ref_o, ref_l = oracle.attention(p)
         gh.assert_parity(o2, l2, ref_o, ref_l, what=f"extend fp8 in-kernel dequantisation {opts}")
+
+
+@pytest.mark.parametrize("opts", [{}, {"window": 4096, "sinks": True}])
+def test_extend_long_context_sampled(opts):
+    # contexts of 20-32K keys: work items of several hundred key tiles; the
+    # oracle checks the first and last rows of each request and a sample
+    ctx = np.array([32000, 20000, 7])
+    ql = np.array([300, 1000, 129])
+    p = _ext(91, Hq=32, Hkv=8, D=128, ps=16, ctx=ctx, ql=ql, **opts)
+    out, lse = gh.run(p)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    qsl = p.query_start_loc
+    rng = np.random.default_rng(6)
+    rows = [int(qsl[b]) for b in range(p.batch)] + [int(qsl[b + 1]) - 1 for b in range(p.batch)]
+    rows += list(rng.choice(p.num_rows, size=24, replace=False))
+    rows = np.unique(np.array(rows, np.int32))
+    ref_o, ref_l = oracle.attention(p, rows=rows)
+    gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what=f"extend long context {opts}")
