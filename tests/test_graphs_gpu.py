@@ -29,15 +29,15 @@ def _decode(seed, lens):
                             pool_pages=POOL, bt_width=WIDTH)
 
 
-def _extend(seed, ctx, ql):
+def _extend(seed, ctx, ql, **kw):
     ctx, ql = np.asarray(ctx), np.asarray(ql)
     return wl.build_problem("extend", num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
-                            seq_lens=ctx + ql, query_lens=ql, seed=seed, pool_pages=POOL, bt_width=WIDTH)
+                            seq_lens=ctx + ql, query_lens=ql, seed=seed, pool_pages=POOL, bt_width=WIDTH, **kw)
 
 
 def _fill(dst, p):
     src = gh.upload(p)
-    for k in ("q", "k", "v", "bt", "sl", "qsl", "sinks"):
+    for k in ("q", "k", "v", "bt", "sl", "qsl", "sinks", "k_scales", "v_scales"):
         if dst.get(k) is not None:
             dst[k].copy_(src[k])
 
@@ -50,7 +50,8 @@ def _graph_roundtrip(first, second):
     scratch = pb.alloc_scratch(plan)
     out = torch.zeros(first.q.shape, dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros(first.q.shape[:2], dtype=torch.float32, device="cuda")
-    kw = dict(scale=first.scale, out=out, lse=lse, sinks=d["sinks"], scratch=scratch)
+    kw = dict(scale=first.scale, out=out, lse=lse, sinks=d["sinks"], scratch=scratch, k_scale=first.k_scale,
+              v_scale=first.v_scale, k_scales=d.get("k_scales"), v_scales=d.get("v_scales"))
 
     def call():
         if first.mode == "decode":
@@ -94,3 +95,16 @@ def test_extend_graph_replay_with_new_batch():
     for p, o, l in ((a, oa, la), (b, ob, lb)):
         ref_o, ref_l = oracle.attention(p)
         gh.assert_parity(o, l, ref_o, ref_l, what="graph replay extend")
+
+
+def test_extend_e4m3_graph_replay_with_new_scales():
+    # e4m3 cache through the bf16 copy (one more captured kernel), per-request
+    # scales read from device memory on every replay
+    a = _extend(521, [100, 0, 700, 1000], [60, 200, 3, 137], kv_dtype="fp8_e4m3",
+                k_scales=[0.05, 0.1, 0.02, 0.07], v_scales=[0.03, 0.2, 0.05, 0.01])
+    b = _extend(522, [0, 950, 20, 333], [150, 50, 150, 50], kv_dtype="fp8_e4m3",
+                k_scales=[0.2, 0.01, 0.06, 0.04], v_scales=[0.1, 0.05, 0.3, 0.02])
+    (oa, la), (ob, lb) = _graph_roundtrip(a, b)
+    for p, o, l in ((a, oa, la), (b, ob, lb)):
+        ref_o, ref_l = oracle.attention(p)
+        gh.assert_parity(o, l, ref_o, ref_l, what="graph replay extend e4m3")
