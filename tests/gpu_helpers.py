@@ -97,5 +97,7 @@ def assert_parity(out, lse, ref_out, ref_lse, what=""):
         assert np.array_equal(np.isneginf(lse), ninf), f"{what}: -inf LSE pattern differs"
         le = np.abs(lse[~ninf].astype(np.float64) - ref_lse[~ninf])
         assert le.size == 0 or le.max() <= LSE_ATOL, f"{what}: LSE max err {le.max():.3e}"
-    return float(err.max()), (float(np.abs(lse.astype(np.float64) - ref_lse)[np.isfinite(ref_lse)].max())
-                              if lse is not None and np.isfinite(ref_lse).any() else 0.0)
+    if lse is None or not np.isfinite(ref_lse).any():
+        return float(err.max()), 0.0
+    fin = np.isfinite(ref_lse)
+    return float(err.max()), float(np.abs(lse[fin].astype(np.float64) - ref_lse[fin]).max())
