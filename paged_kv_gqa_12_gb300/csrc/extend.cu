@@ -35,6 +35,12 @@
 //     inside the last page are zeroed, so stale or NaN slots never meet P = 0.
 //   * A one-CTA scheduler kernel builds the (request, query tile) list from
 //     the device metadata, heaviest first; CTA i takes item i / Hkv.
+//   * e4m3 cache: a call first writes bf16(float(code) * scale) of every
+//     attended page into a copy in the scratch workspace
+//     (extend_kv_copy_kernel) and this kernel reads the copy; plans whose
+//     copy would not fit dequantise each tile in shared memory instead (the
+//     TMA producer warps convert it in place).  Either way the MMAs see the
+//     same bf16 values.
 #include <climits>
 #include <cmath>
 #include <cstdint>
