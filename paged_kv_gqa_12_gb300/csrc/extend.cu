@@ -21,9 +21,10 @@
 //     next tile's QK), warps 3-6 run the softmax with one TMEM lane (= one
 //     query row) per thread.  Two CTAs share an SM where TMEM and shared
 //     memory allow.
-//   * S = Q K^T (M=128, N=BN keys) lands in one of two TMEM buffers, so the
-//     next tile's QK overlaps this tile's softmax (a buffer is reused once
-//     the PV that read its P has completed); P (bf16) is written back
+//   * S = Q K^T (M=128, N=BN keys) lands in one of NSB TMEM buffers (as
+//     many as fit beside O: 2 for head_dim 128), so the next tiles' QK
+//     overlaps this tile's softmax (a buffer is reused once the PV that read
+//     its P has completed); P (bf16) is written back
 //     over S and consumed from TMEM by O += P V (V read MN-major from shared
 //     memory); O stays in TMEM for the whole key loop.
 //   * Online softmax in the log2 domain with lazy rescaling: O and l are
@@ -231,9 +232,6 @@ struct ExtTraits {
   static constexpr int KV_CHUNK = BN * 128;
   static constexpr int TILE = NCH * KV_CHUNK;        // K (or V) tile
   static constexpr int SMEM_DATA = Q_BYTES + 2 * NST * TILE;  // Q, K ring, V ring
-  // mbarriers: q_full, six per ring stage, s_full/p_full/o_done pairs; then the TMEM address
-  static constexpr int BAR_BYTES = ((1 + 6 * NST + 6) * 8 + 4 + 15) / 16 * 16;
-  static constexpr int SMEM = 1024 + SMEM_DATA + BAR_BYTES;   // 1024: alignment slack for SW128
   // fp8 cache: the e4m3 tile lands in the second half of the bf16 stage
   // buffer, rows of RB8 bytes (row r under bf16 row r's upper chunks when
   // D >= 128), and is dequantised in place
@@ -241,8 +239,15 @@ struct ExtTraits {
   static constexpr int NCC8 = D / RB8;               // fp8 boxes per page
   static constexpr int F8_OFF = TILE / 2;
   static constexpr uint32_t TMEM_COLS = 512 / CPS;   // CPS CTAs share an SM's 512 columns
-  static constexpr uint32_t TMEM_O = 2 * BN;         // two S buffers, then O
-  static_assert(2 * BN + D <= static_cast<int>(TMEM_COLS), "TMEM plan: S0, S1, O");
+  // S buffers: as many as the columns left beside O hold (2 for head_dim
+  // 128, 3 for 64, 4 for 256 with one CTA per SM); QK runs up to NSB - 1
+  // tiles ahead of the softmax
+  static constexpr int NSB = (static_cast<int>(TMEM_COLS) - D) / BN;
+  static constexpr uint32_t TMEM_O = NSB * BN;       // S buffers, then O
+  static_assert(NSB >= 2 && NSB * BN + D <= static_cast<int>(TMEM_COLS), "TMEM plan: S buffers, O");
+  // mbarriers: q_full, six per ring stage, s_full/p_full/o_done per S buffer; then the TMEM address
+  static constexpr int BAR_BYTES = ((1 + 6 * NST + 3 * NSB) * 8 + 4 + 15) / 16 * 16;
+  static constexpr int SMEM = 1024 + SMEM_DATA + BAR_BYTES;   // 1024: alignment slack for SW128
   static_assert(CPS * SMEM <= 232448, "shared memory for CPS CTAs per SM");
   static_assert(BN % 64 == 0, "P is stored 32 columns (64 keys) at a time");
 };
@@ -342,9 +347,9 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   uint64_t* k_land = v_empty + NST;   // fp8: the e4m3 tile has landed (before dequantisation)
   uint64_t* v_land = k_land + NST;
   uint64_t* s_full = v_land + NST;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + 2);
+  uint64_t* p_full = s_full + T::NSB;
+  uint64_t* o_done = p_full + T::NSB;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + T::NSB);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -361,7 +366,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       mbar_init(&k_land[i], 1);
       mbar_init(&v_land[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < T::NSB; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);
       mbar_init(&o_done[i], 1);
@@ -455,11 +460,11 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       for (int j = 0; j < n && ok; ++j) {
         const int stage = j % NST;
         ok = wait_or_abort(&k_full[stage], (j / NST) & 1, p.err);
-        // S buffer j & 1 holds P of tile j - 2 until the PV that reads it has completed
-        if (ok && j >= 2) ok = wait_or_abort(&o_done[j & 1], ((j - 2) >> 1) & 1, p.err);
+        // S buffer j % NSB holds P of tile j - NSB until the PV that reads it has completed
+        if (ok && j >= T::NSB) ok = wait_or_abort(&o_done[j % T::NSB], ((j / T::NSB) - 1) & 1, p.err);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t tS = tbase + static_cast<uint32_t>((j & 1) * BN);
+        const uint32_t tS = tbase + static_cast<uint32_t>((j % T::NSB) * BN);
         const uint32_t k_u = k_ring + stage * T::TILE;
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
@@ -467,7 +472,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
           const uint64_t bd = sdesc_sw128(k_u + (s >> 2) * T::KV_CHUNK + (s & 3) * 32, 16, 1024);
           umma_ss(tS, ad, bd, idesc_qk, s > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[j & 1]);
+        umma_commit(&s_full[j % T::NSB]);
         umma_commit(&k_empty[stage]);
       }
     }
@@ -481,11 +486,11 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       bool ok = true;
       for (int jj = 0; jj < n && ok; ++jj) {
         const int st = jj % NST;
-        ok = wait_or_abort(&p_full[jj & 1], (jj >> 1) & 1, p.err) &&
+        ok = wait_or_abort(&p_full[jj % T::NSB], (jj / T::NSB) & 1, p.err) &&
              wait_or_abort(&v_full[st], (jj / NST) & 1, p.err);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t tP = tbase + static_cast<uint32_t>((jj & 1) * BN);
+        const uint32_t tP = tbase + static_cast<uint32_t>((jj % T::NSB) * BN);
         const uint32_t v_u = v_ring + st * T::TILE;
         // P columns: k-step s (16 keys) at column 8s; on split tiles P_hi at
         // 16s and P_lo at 16s + 8
@@ -503,7 +508,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
             umma_ts(tbase + T::TMEM_O, tP + s * 16 + 8, bd, idesc_pv, 1u);
           }
         }
-        umma_commit(&o_done[jj & 1]);
+        umma_commit(&o_done[jj % T::NSB]);
         umma_commit(&v_empty[st]);
       }
     }
@@ -527,10 +532,10 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const int k0 = (kt0 + j) * BN;
-      ok = __all_sync(0xffffffffu, wait_or_abort(&s_full[j & 1], (j >> 1) & 1, p.err));
+      ok = __all_sync(0xffffffffu, wait_or_abort(&s_full[j % T::NSB], (j / T::NSB) & 1, p.err));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tS = tbase + lane_off + static_cast<uint32_t>((j & 1) * BN);
+      const uint32_t tS = tbase + lane_off + static_cast<uint32_t>((j % T::NSB) * BN);
       uint32_t sr[BN];
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
@@ -618,7 +623,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       tmem_wait_st();
       if (any_need && j > 0) {
         // O must hold PV of tile j-1 before it is rescaled (and no PV may run meanwhile)
-        ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.err));
+        ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[(j - 1) % T::NSB], ((j - 1) / T::NSB) & 1, p.err));
         if (!ok) break;
         tc_fence_after();
         const uint32_t tO = tbase + lane_off + T::TMEM_O;
@@ -656,9 +661,10 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[j & 1]);
+      if (lane == 0) mbar_arrive(&p_full[j % T::NSB]);
     }
-    if (ok && n > 0) ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, p.err));
+    if (ok && n > 0)
+      ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[(n - 1) % T::NSB], ((n - 1) / T::NSB) & 1, p.err));
     if (ok) {
       tc_fence_after();
       const int hq = kvh * G + hh;
