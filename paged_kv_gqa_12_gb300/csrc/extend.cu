@@ -245,6 +245,14 @@ struct ExtTraits {
   static constexpr int NSB = (static_cast<int>(TMEM_COLS) - D) / BN;
   static constexpr uint32_t TMEM_O = NSB * BN;       // S buffers, then O
   static_assert(NSB >= 2 && NSB * BN + D <= static_cast<int>(TMEM_COLS), "TMEM plan: S buffers, O");
+  // S buffer of tile j and the phase parity of its barriers (unsigned: a
+  // power-of-two count reduces to a mask and a shift)
+  __device__ static __forceinline__ int sbuf(int j) {
+    return static_cast<int>(static_cast<unsigned>(j) % static_cast<unsigned>(NSB));
+  }
+  __device__ static __forceinline__ uint32_t sphase(int j) {
+    return (static_cast<unsigned>(j) / static_cast<unsigned>(NSB)) & 1u;
+  }
   // mbarriers: q_full, six per ring stage, s_full/p_full/o_done per S buffer; then the TMEM address
   static constexpr int BAR_BYTES = ((1 + 6 * NST + 3 * NSB) * 8 + 4 + 15) / 16 * 16;
   static constexpr int SMEM = 1024 + SMEM_DATA + BAR_BYTES;   // 1024: alignment slack for SW128
@@ -461,10 +469,10 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         const int stage = j % NST;
         ok = wait_or_abort(&k_full[stage], (j / NST) & 1, p.err);
         // S buffer j % NSB holds P of tile j - NSB until the PV that reads it has completed
-        if (ok && j >= T::NSB) ok = wait_or_abort(&o_done[j % T::NSB], ((j / T::NSB) - 1) & 1, p.err);
+        if (ok && j >= T::NSB) ok = wait_or_abort(&o_done[T::sbuf(j)], T::sphase(j - T::NSB), p.err);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t tS = tbase + static_cast<uint32_t>((j % T::NSB) * BN);
+        const uint32_t tS = tbase + static_cast<uint32_t>(T::sbuf(j) * BN);
         const uint32_t k_u = k_ring + stage * T::TILE;
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
@@ -472,7 +480,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
           const uint64_t bd = sdesc_sw128(k_u + (s >> 2) * T::KV_CHUNK + (s & 3) * 32, 16, 1024);
           umma_ss(tS, ad, bd, idesc_qk, s > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[j % T::NSB]);
+        umma_commit(&s_full[T::sbuf(j)]);
         umma_commit(&k_empty[stage]);
       }
     }
@@ -486,11 +494,11 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       bool ok = true;
       for (int jj = 0; jj < n && ok; ++jj) {
         const int st = jj % NST;
-        ok = wait_or_abort(&p_full[jj % T::NSB], (jj / T::NSB) & 1, p.err) &&
+        ok = wait_or_abort(&p_full[T::sbuf(jj)], T::sphase(jj), p.err) &&
              wait_or_abort(&v_full[st], (jj / NST) & 1, p.err);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t tP = tbase + static_cast<uint32_t>((jj % T::NSB) * BN);
+        const uint32_t tP = tbase + static_cast<uint32_t>(T::sbuf(jj) * BN);
         const uint32_t v_u = v_ring + st * T::TILE;
         // P columns: k-step s (16 keys) at column 8s; on split tiles P_hi at
         // 16s and P_lo at 16s + 8
@@ -508,7 +516,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
             umma_ts(tbase + T::TMEM_O, tP + s * 16 + 8, bd, idesc_pv, 1u);
           }
         }
-        umma_commit(&o_done[jj % T::NSB]);
+        umma_commit(&o_done[T::sbuf(jj)]);
         umma_commit(&v_empty[st]);
       }
     }
@@ -532,10 +540,10 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const int k0 = (kt0 + j) * BN;
-      ok = __all_sync(0xffffffffu, wait_or_abort(&s_full[j % T::NSB], (j / T::NSB) & 1, p.err));
+      ok = __all_sync(0xffffffffu, wait_or_abort(&s_full[T::sbuf(j)], T::sphase(j), p.err));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tS = tbase + lane_off + static_cast<uint32_t>((j % T::NSB) * BN);
+      const uint32_t tS = tbase + lane_off + static_cast<uint32_t>(T::sbuf(j) * BN);
       uint32_t sr[BN];
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
@@ -623,7 +631,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       tmem_wait_st();
       if (any_need && j > 0) {
         // O must hold PV of tile j-1 before it is rescaled (and no PV may run meanwhile)
-        ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[(j - 1) % T::NSB], ((j - 1) / T::NSB) & 1, p.err));
+        ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[T::sbuf(j - 1)], T::sphase(j - 1), p.err));
         if (!ok) break;
         tc_fence_after();
         const uint32_t tO = tbase + lane_off + T::TMEM_O;
@@ -661,10 +669,10 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[j % T::NSB]);
+      if (lane == 0) mbar_arrive(&p_full[T::sbuf(j)]);
     }
     if (ok && n > 0)
-      ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[(n - 1) % T::NSB], ((n - 1) / T::NSB) & 1, p.err));
+      ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[T::sbuf(n - 1)], T::sphase(n - 1), p.err));
     if (ok) {
       tc_fence_after();
       const int hq = kvh * G + hh;
