@@ -27,7 +27,8 @@
  * ctx_b = seq_lens[b] - (query_start_loc[b+1] - query_start_loc[b]); the new
  * tokens' K/V must already be in the pages.
  * fp8 KV: element value = bf16( float(e4m3) * k_scale ) (same for V with
- * v_scale), as the prefix-prefill page dequantises.
+ * v_scale; per-request scales k_scales[b] / v_scales[b] replace them when
+ * given), as the prefix-prefill page dequantises.
  *
  * Conventions
  *   - Pointers named "device" must be device memory of the current device;
@@ -122,7 +123,9 @@ pa_status pa_plan(const pa_shape* shape, const int32_t* host_seq_lens, int32_t b
                   pa_plan_t* plan);
 
 /* Split-KV paged decode: stage 1 (per-split partial output and LSE, written to
- * the scratch workspace) followed by the LSE merge (final out / lse).
+ * the scratch workspace) followed by the LSE merge (final out / lse).  When
+ * the plan gives every request a single split (plan->max_splits == 1) stage 1
+ * writes out / lse itself and the merge is not launched (plan->launches).
  *   q            device bf16, [batch, Hq, D], strides q_stride_tok / q_stride_head
  *   k_cache, v_cache  device, [num_pages, page_size, Hkv, D] bf16 or e4m3 bytes,
  *                strides kv_stride_page / kv_stride_tok / kv_stride_head
@@ -163,7 +166,8 @@ pa_status pa_decode(const pa_plan_t* plan,
  * device memory for a scratch buffer -- for example a plugin or host runtime
  * with no device allocator of its own, a process whose memory pool already
  * owns the whole GPU, or code that must never allocate so that its latency
- * stays fixed.  Arguments and results are those of pa_decode, minus scratch.
+ * stays fixed.  Arguments and results are those of pa_decode, minus scratch
+ * and the per-request scales (per-tensor k_scale / v_scale only).
  *   - The workspace is a 16 MiB array inside the library's device image,
  *     present on every GPU that loads the library until the process exits.
  *     Plans whose scratch_bytes exceed 16 MiB return PA_ERR_SCRATCH_TOO_SMALL.
@@ -242,8 +246,10 @@ pa_status pa_append_kv(const void* k_new, const void* v_new, int64_t new_stride_
 pa_status pa_scratch_init(void* scratch, void* stream);
 
 /* Synchronise `stream`, read and clear the scratch error header.  Returns
- * PA_OK, PA_ERR_DEVICE (a kernel's bounded wait expired; the header's code is
- * stored in *device_code when non-NULL) or PA_ERR_CUDA. */
+ * PA_OK, PA_ERR_DEVICE (a kernel reported an error: a bounded wait expired,
+ * a length or packing beyond what the plan allows, a work list over its
+ * capacity, a slot outside the pool; the header's code bits are stored in
+ * *device_code when non-NULL) or PA_ERR_CUDA. */
 pa_status pa_check(void* scratch, void* stream, uint32_t* device_code);
 
 /* Static string for a status code. */
