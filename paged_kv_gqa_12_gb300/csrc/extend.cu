@@ -224,6 +224,25 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
   return true;
 }
 
+// The same bounded wait by polling, for the two MMA-issuing threads: they
+// react to a completed phase without a wake-up delay (measured +0.7 % over
+// the suspending wait), and only one thread of each polls.
+__device__ __forceinline__ bool poll_or_abort(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (!mbar_test_wait(bar, parity)) {
+    if ((++spins & 255u) == 0) {
+      if (*reinterpret_cast<volatile uint32_t*>(err) != 0u) return false;
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        atomicOr(err, kErrWaitTimeout);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
 template <int D, int BN, int NST, int CPS, bool FP8 = false>
 struct ExtTraits {
   static constexpr int NCH = D / 64;                 // 128-byte column chunks per row
@@ -467,9 +486,9 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       tc_fence_after();
       for (int j = 0; j < n && ok; ++j) {
         const int stage = j % NST;
-        ok = wait_or_abort(&k_full[stage], (j / NST) & 1, p.err);
+        ok = poll_or_abort(&k_full[stage], (j / NST) & 1, p.err);
         // S buffer j % NSB holds P of tile j - NSB until the PV that reads it has completed
-        if (ok && j >= T::NSB) ok = wait_or_abort(&o_done[T::sbuf(j)], T::sphase(j - T::NSB), p.err);
+        if (ok && j >= T::NSB) ok = poll_or_abort(&o_done[T::sbuf(j)], T::sphase(j - T::NSB), p.err);
         if (!ok) break;
         tc_fence_after();
         const uint32_t tS = tbase + static_cast<uint32_t>(T::sbuf(j) * BN);
@@ -494,8 +513,8 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       bool ok = true;
       for (int jj = 0; jj < n && ok; ++jj) {
         const int st = jj % NST;
-        ok = wait_or_abort(&p_full[T::sbuf(jj)], T::sphase(jj), p.err) &&
-             wait_or_abort(&v_full[st], (jj / NST) & 1, p.err);
+        ok = poll_or_abort(&p_full[T::sbuf(jj)], T::sphase(jj), p.err) &&
+             poll_or_abort(&v_full[st], (jj / NST) & 1, p.err);
         if (!ok) break;
         tc_fence_after();
         const uint32_t tP = tbase + static_cast<uint32_t>(T::sbuf(jj) * BN);
