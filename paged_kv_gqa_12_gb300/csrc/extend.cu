@@ -125,26 +125,26 @@ __global__ void __launch_bounds__(kSchedThreads) extend_schedule_kernel(const Ex
   for (int i = tid; i < kBuckets; i += kSchedThreads) s_hist[i] = 0;
   if (tid == 0) s_total = 0;
   __syncthreads();
-  const int per = (p.batch + kSchedThreads - 1) / kSchedThreads;
-  const int b0 = min(p.batch, tid * per);
-  const int b1 = min(p.batch, b0 + per);
-  int local = 0;
-  for (int b = b0; b < b1; ++b) {
+  // one warp per request, its lanes over the request's query tiles: the
+  // attention kernel waits for this list, so it is built in few rounds
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  constexpr int kSchedWarps = kSchedThreads / 32;
+  for (int b = warp; b < p.batch; b += kSchedWarps) {
     const int qs = p.qsl[b];
     const int qlen = p.qsl[b + 1] - qs;
     const int L = p.seq_lens[b];
     if (qlen == 0) continue;
     if (qlen < 0 || L < qlen || L > p.max_kv || qs < 0 || qs + qlen > p.total_q) {
-      atomicOr(p.err, kErrCapacity);
+      if (lane == 0) atomicOr(p.err, kErrCapacity);
       continue;
     }
     const int nmt = (qlen + p.tm - 1) / p.tm;
-    for (int mt = 0; mt < nmt; ++mt) {
+    for (int mt = lane; mt < nmt; mt += 32) {
       atomicAdd(&s_hist[min(tile_cost(L - qlen, qlen, mt, p.tm, p.window, p.block_n), kBuckets - 1)], 1);
     }
-    local += nmt;
+    if (lane == 0) atomicAdd(&s_total, nmt);
   }
-  atomicAdd(&s_total, local);
   __syncthreads();
   // descending exclusive scan: heaviest class first (one warp, 8 classes per lane)
   if (tid < 32) {
@@ -170,13 +170,13 @@ __global__ void __launch_bounds__(kSchedThreads) extend_schedule_kernel(const Ex
     }
   }
   __syncthreads();
-  for (int b = b0; b < b1; ++b) {
+  for (int b = warp; b < p.batch; b += kSchedWarps) {
     const int qs = p.qsl[b];
     const int qlen = p.qsl[b + 1] - qs;
     const int L = p.seq_lens[b];
     if (qlen <= 0 || L < qlen || L > p.max_kv || qs < 0 || qs + qlen > p.total_q) continue;
     const int nmt = (qlen + p.tm - 1) / p.tm;
-    for (int mt = 0; mt < nmt; ++mt) {
+    for (int mt = lane; mt < nmt; mt += 32) {
       const int pos = atomicAdd(&s_off[min(tile_cost(L - qlen, qlen, mt, p.tm, p.window, p.block_n), kBuckets - 1)], 1);
       if (pos < p.work_cap) p.work[pos] = make_int2(b, mt);
     }
