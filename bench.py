@@ -339,7 +339,7 @@ def run_ours(args):
         kernels["decode"] = {"bound": "hbm", "achieved": round(dec_ach, 1), "peak": hbm, "unit": "GB/s",
                              "frac": round(dec_ach / hbm, 4),
                              "traffic": recorded_traffic("decode_split_kernel", ["decode.cu", "ptx.cuh", "pa_internal.h"]),
-                             "timed": "pa_decode call (split kernel + merge kernel), CUDA events, mean over steps",
+                             "timed": "pa_decode call (split kernel; the last split of each request and kv head merges), CUDA events, mean over steps",
                              "algorithmic_bytes_per_launch": dbytes, "peak_source": f"{peak_src} hbm_gbs"}
     if extend_ok:
         ext_mean = statistics.mean(ext_ms) / 1e3

@@ -104,14 +104,19 @@ typedef struct {
   int32_t bt_cache;           /* block-table entries staged in shared memory per CTA */
   int32_t smem_bytes;         /* dynamic shared memory per CTA */
   int32_t grid[3];            /* main kernel grid */
-  int64_t scratch_bytes;      /* device scratch the calls need (>= 256) */
+  int64_t scratch_bytes;      /* device scratch the calls need (>= 65536, the header) */
   int32_t launches;           /* kernel launches one call makes */
   int32_t kv_copy;            /* extend over an e4m3 cache: 1 = each call first dequantises the
                                  pages it reads, once, into a bf16 copy inside the scratch
                                  workspace and attends over the copy (chosen while the copy
                                  for max_batch x max_pages_per_seq pages fits in 2 GiB);
                                  0 = every attention CTA dequantises its tiles in shared memory */
-  int32_t reserved[6];
+  int32_t split_merge;        /* decode / verify with max_splits > 1: 1 = the split that finishes
+                                 last for a (request, kv head) merges that pair's splits, counted
+                                 by arrival counters in the scratch header (one launch; chosen
+                                 while max_batch x Hkv x head groups <= 16320); 0 = a merge
+                                 kernel follows */
+  int32_t reserved[5];
 } pa_plan_t;
 
 /* Plan a decode or extend call from capacities.  host_seq_lens (host memory,
@@ -125,7 +130,9 @@ pa_status pa_plan(const pa_shape* shape, const int32_t* host_seq_lens, int32_t b
 /* Split-KV paged decode: stage 1 (per-split partial output and LSE, written to
  * the scratch workspace) followed by the LSE merge (final out / lse).  When
  * the plan gives every request a single split (plan->max_splits == 1) stage 1
- * writes out / lse itself and the merge is not launched (plan->launches).
+ * writes out / lse itself; with plan->split_merge the stage-1 CTA that
+ * finishes last for a (request, kv head) merges its splits; otherwise a merge
+ * kernel follows (plan->launches).
  *   q            device bf16, [batch, Hq, D], strides q_stride_tok / q_stride_head
  *   k_cache, v_cache  device, [num_pages, page_size, Hkv, D] bf16 or e4m3 bytes,
  *                strides kv_stride_page / kv_stride_tok / kv_stride_head
@@ -145,8 +152,9 @@ pa_status pa_plan(const pa_shape* shape, const int32_t* host_seq_lens, int32_t b
  *   out          device bf16 [batch, Hq, D], strides out_stride_tok / out_stride_head
  *   lse          device fp32 [batch, Hq] contiguous, or NULL
  *   scratch      device, >= plan->scratch_bytes bytes, 256-byte aligned; its
- *                first 256 bytes are the error header (zero it once with
- *                pa_scratch_init).  Contents are overwritten by every call.
+ *                first 64 KiB are the header (error word and split-arrival
+ *                counters; zero it once with pa_scratch_init).  The rest is
+ *                overwritten by every call.
  * Concurrent calls must not share a scratch buffer. */
 pa_status pa_decode(const pa_plan_t* plan,
                     const void* q, int64_t q_stride_tok, int64_t q_stride_head,
@@ -241,11 +249,16 @@ pa_status pa_append_kv(const void* k_new, const void* v_new, int64_t new_stride_
                        int32_t kv_dtype, const int64_t* slot_mapping, int32_t num_tokens,
                        float k_scale, float v_scale, void* scratch, void* stream);
 
-/* Zero the 256-byte error header at the start of a scratch buffer (enqueued
- * on `stream`).  Call once after allocating the scratch. */
+/* Zero the 64 KiB header at the start of a scratch buffer (enqueued on
+ * `stream`): the error word, and the split-arrival counters that decode
+ * calls leave at zero when they finish.  Call once after allocating the
+ * scratch. */
 pa_status pa_scratch_init(void* scratch, void* stream);
 
-/* Synchronise `stream`, read and clear the scratch error header.  Returns
+/* Synchronise `stream`, read the scratch error word and, if it is set,
+ * zero the whole header (a failed call can leave arrival counters behind:
+ * call pa_check, or pa_scratch_init, before reusing a scratch buffer after
+ * a device error).  Returns
  * PA_OK, PA_ERR_DEVICE (a kernel reported an error: a bounded wait expired,
  * a length or packing beyond what the plan allows, a work list over its
  * capacity, a slot outside the pool; the header's code bits are stored in

@@ -21,6 +21,12 @@ PA_ERR_SCRATCH_TOO_SMALL = 3
 PA_ERR_CUDA = 4
 PA_ERR_DEVICE = 5
 
+# bytes of the scratch header (error word, then split-arrival counters) at
+# the start of every scratch workspace
+SCRATCH_HEADER_BYTES = 65536
+# (request, kv head group) pairs a plan may have for its last split to merge
+MERGE_COUNTERS = (SCRATCH_HEADER_BYTES - 256) // 4
+
 MODE_DECODE = 0
 MODE_EXTEND = 1
 MODE_VERIFY = 2
@@ -65,7 +71,8 @@ class PaPlan(ctypes.Structure):
         ("scratch_bytes", ctypes.c_int64),
         ("launches", ctypes.c_int32),
         ("kv_copy", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 6),
+        ("split_merge", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 5),
     ]
 
 

@@ -110,14 +110,21 @@ pa_status plan_decode(const pa_shape& s, const int32_t* host_lens, int32_t batch
       units = static_cast<int64_t>(s.max_batch) * s.num_kv_heads * hgroups * max_tiles;
     }
     const int ctas_per_sm = (decode_config(s.head_dim, fp8, rows, 64).smem_bytes * 2 <= kMaxSmemPerCta) ? 2 : 1;
-    const int64_t target = static_cast<int64_t>(num_sms) * ctas_per_sm * 4;
-    split_tiles = std::max<int64_t>(8, cdiv64(units, std::max<int64_t>(target, 1)));
-    // When the (request, head) pairs alone fill a wave, a split holds at
-    // least 1024 keys: shorter ones spend more on their prologue and the
-    // merge than they gain in balance (e4m3 window-1024 workload: one split
-    // 2.30 TB/s, two 2.05).
+    const int64_t slots = static_cast<int64_t>(num_sms) * ctas_per_sm;
     const int64_t pairs = static_cast<int64_t>(host_lens ? batch : s.max_batch) * s.num_kv_heads * hgroups;
-    if (pairs >= static_cast<int64_t>(num_sms) * ctas_per_sm) split_tiles = std::max<int64_t>(split_tiles, cdiv64(1024, TS));
+    // Splits per CTA slot: about four; once the (request, head) pairs alone
+    // fill a wave, about eight, but each split then holds at least 1024 keys
+    // per 8 query rows (fewer, longer splits cost less in prologues, partial
+    // outputs and merging than they gain in balance).  Measured, with equal
+    // splits per request: Llama-3-8B-shaped decode 0.1897 ms at four,
+    // 0.1863 at eight (1024-key splits); its first 16 requests 0.0681 at
+    // four, 0.0748 at eight; its verify form (4 tokens, 16 rows) 0.2127 with
+    // 118-tile splits, 0.2196 with 1024-key ones; e4m3 window-1024 workload:
+    // one split 2.30 TB/s, two 2.05.
+    const bool wave = pairs >= slots;
+    const int64_t target = slots * (wave ? 8 : 4);
+    split_tiles = std::max<int64_t>(8, cdiv64(units, std::max<int64_t>(target, 1)));
+    if (wave) split_tiles = std::max<int64_t>(split_tiles, cdiv64(1024 * std::max(1, rows / 8), TS));
     // no second split of a single tile (a window start off the tile grid)
     if (split_tiles + 1 >= max_tiles) split_tiles = max_tiles;
     split_tiles = std::min<int64_t>(split_tiles, max_tiles);
@@ -141,7 +148,12 @@ pa_status plan_decode(const pa_shape& s, const int32_t* host_lens, int32_t batch
   out->grid[2] = s.max_batch;
   const int64_t prow = static_cast<int64_t>(s.max_batch) * qlen * s.num_q_heads * max_splits;
   out->scratch_bytes = kScratchHeaderBytes + align_up(prow * s.head_dim * 4, 256) + align_up(prow * 4, 256);
-  out->launches = max_splits > 1 ? 2 : 1;  // split kernel (+ merge kernel when a request can have several splits)
+  // several splits: the last split of each (request, kv head group) merges
+  // them while the header has a counter for every such pair, else a merge
+  // kernel follows the split kernel
+  const int64_t pairs_cap = static_cast<int64_t>(s.max_batch) * s.num_kv_heads * hgroups;
+  out->split_merge = (max_splits > 1 && pairs_cap <= kMergeCounters) ? 1 : 0;
+  out->launches = (max_splits > 1 && !out->split_merge) ? 2 : 1;
   return PA_OK;
 }
 
@@ -222,7 +234,7 @@ using namespace pa;
 
 extern "C" {
 
-int32_t pa_version(void) { return 102; }
+int32_t pa_version(void) { return 103; }
 
 const char* pa_status_string(pa_status status) {
   switch (status) {
@@ -360,6 +372,7 @@ pa_status run_split_kv(const pa_plan_t* plan, const void* q, int64_t q_stride_to
   p.q_len = qlen;
   p.head_groups = hgroups;
   p.qsl = qsl;
+  p.merge_cnt = plan->split_merge ? reinterpret_cast<uint32_t*>(sc + kMergeCounterOffset) : nullptr;
   p.err = reinterpret_cast<uint32_t*>(sc);
   const dim3 grid(plan->max_splits, s.num_kv_heads * hgroups, batch);
   const cudaError_t e = launch_decode(cfg, tmk, tmv, p, grid, static_cast<cudaStream_t>(stream));
@@ -384,7 +397,8 @@ pa_status pa_check(void* scratch, void* stream, uint32_t* device_code) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
   if (device_code) *device_code = word;
   if (word == 0) return PA_OK;
-  if (cudaMemsetAsync(scratch, 0, sizeof word, st) != cudaSuccess) return PA_ERR_CUDA;
+  // a failed call may leave split-arrival counters behind: clear the whole header
+  if (cudaMemsetAsync(scratch, 0, kScratchHeaderBytes, st) != cudaSuccess) return PA_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
   return PA_ERR_DEVICE;
 }

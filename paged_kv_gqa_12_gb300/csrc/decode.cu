@@ -27,7 +27,11 @@
 //   * Online softmax in the log2 domain; per-thread partial row sums are
 //     reduced once at the end; the 4 warps' states are merged in shared
 //     memory.  A request with one split writes the final output directly;
-//     otherwise the merge kernel combines the splits.
+//     otherwise each split writes its normalised partial and LSE, and the
+//     split that finishes last for its (request, kv head) -- counted by an
+//     atomic arrival counter in the scratch header -- merges them, so a call
+//     is one launch.  Plans with more (request, kv head) pairs than the
+//     header holds counters use the separate merge kernel instead.
 #include <cfloat>
 #include <cstdint>
 #include <type_traits>
@@ -70,6 +74,11 @@ __device__ __forceinline__ SplitRange split_range(const DecodeParams& p, int L) 
   r.n_tiles = (r.hi + ts - 1) / ts - r.tile0;
   r.tiles_per_split = p.fixed_splits > 0 ? (r.n_tiles + p.fixed_splits - 1) / p.fixed_splits : p.split_tiles;
   r.n_splits = (r.n_tiles + r.tiles_per_split - 1) / r.tiles_per_split;
+  // equal splits (a request of 4.5 split lengths gets five of 0.9, not four
+  // full ones and a half): no split is longer than planned, and the CTAs a
+  // request contributes to the last wave are all short
+  r.tiles_per_split = (r.n_tiles + r.n_splits - 1) / r.n_splits;
+  r.n_splits = (r.n_tiles + r.tiles_per_split - 1) / r.tiles_per_split;
   return r;
 }
 
@@ -98,6 +107,66 @@ struct Traits {
     return static_cast<uint32_t>(cc * (TS * RB) + row * RB) + ((((x >> 4) ^ sw) << 4) | (x & 15));
   }
 };
+
+// LSE merge of one request's splits for the R rows (token, head) of one kv
+// head group, by the CTA that finished last: thread t takes 4 consecutive
+// dims of one row; the splits are folded eight at a time (their loads in
+// flight together) into a running maximum, sum and weighted output.  The
+// partials are read from L2: other SMs wrote them.
+template <int D>
+__device__ __forceinline__ void merge_splits(const DecodeParams& p, int n_splits, int R, int Gc, int hq0,
+                                             int64_t qrow0) {
+  constexpr int C = D / 4;   // float4 chunks per row
+  constexpr int U = 8;
+  for (int e = threadIdx.x; e < R * C; e += kWarps * 32) {
+    const int h = e / C;
+    const int d = (e - h * C) * 4;
+    const int tq = h / Gc;
+    const int hq = hq0 + (h - tq * Gc);
+    const int64_t orow = qrow0 + tq;
+    const int64_t row0 = (orow * p.num_q_heads + hq) * p.max_splits;
+    const float* lp = p.lse_part + row0;
+    const float* op = p.o_part + row0 * D + d;
+    const bool has_sink = p.sinks != nullptr;
+    float M = has_sink ? p.sinks[hq] * kLog2e : -INFINITY;
+    float Z = has_sink ? 1.f : 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < n_splits; s0 += U) {
+      float l[U];
+      float4 o[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const bool ok = s0 + u < n_splits;
+        l[u] = ok ? __ldcg(lp + s0 + u) * kLog2e : -INFINITY;
+        o[u] = ok ? __ldcg(reinterpret_cast<const float4*>(op + static_cast<int64_t>(s0 + u) * D))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float mx = l[0];
+#pragma unroll
+      for (int u = 1; u < U; ++u) mx = fmaxf(mx, l[u]);
+      if (mx > M) {   // rescale what was summed against the old maximum
+        const float f = ex2(M - mx);
+        Z *= f;
+        acc.x *= f; acc.y *= f; acc.z *= f; acc.w *= f;
+        M = mx;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (l[u] == -INFINITY) continue;   // padding, or a split with no key for this row
+        const float w = ex2(l[u] - M);
+        Z += w;
+        acc.x += w * o[u].x; acc.y += w * o[u].y; acc.z += w * o[u].z; acc.w += w * o[u].w;
+      }
+    }
+    const float inv = Z > 0.f ? 1.f / Z : 0.f;
+    uint16_t* outp = p.out + orow * p.out_stride_tok + static_cast<int64_t>(hq) * p.out_stride_head + d;
+    // (rows are 4-byte aligned: two bf16 pairs)
+    reinterpret_cast<uint32_t*>(outp)[0] = pack_bf16x2(acc.x * inv, acc.y * inv);
+    reinterpret_cast<uint32_t*>(outp)[1] = pack_bf16x2(acc.z * inv, acc.w * inv);
+    if (d == 0 && p.lse != nullptr)
+      p.lse[orow * p.num_q_heads + hq] = M == -INFINITY ? -INFINITY : (M + lg2(Z)) * kLn2;
+  }
+}
 
 template <int D, bool FP8, int NH8, int TS, int NS>
 __global__ void __launch_bounds__(kWarps * 32)
@@ -143,7 +212,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
   }
   const int tile_begin = r.tile0 + split * r.tiles_per_split;
   const int tile_end = min(tile_begin + r.tiles_per_split, r.tile0 + r.n_tiles);
-  const int n_tiles = tile_end - tile_begin;
   const int tok_lo = max(r.lo, tile_begin * TS);
   const int tok_hi = min(r.hi, tile_end * TS);
   const int ps = p.page_size;
@@ -171,12 +239,13 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
   const int g = lane >> 2;   // MMA group id
   const int c = lane & 3;    // thread in group
 
-  if (pg1 - pg0 > p.bt_cache) {  // planner invariant; never expected
-    if (tid == 0) atomicOr(p.err, kErrSchedOverflow);
-    return;
-  }
+  // planner invariant, never expected to fail; a split that fails it reads
+  // nothing but still reports to the merge, so the arrival count completes
+  const bool bt_fits = pg1 - pg0 <= p.bt_cache;
+  if (!bt_fits && tid == 0) atomicOr(p.err, kErrSchedOverflow);
+  const int n_tiles = bt_fits ? tile_end - tile_begin : 0;
   const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-  for (int i = tid; i < pg1 - pg0; i += kWarps * 32) bt_s[i] = bt_row[pg0 + i];
+  for (int i = tid; i < (bt_fits ? pg1 - pg0 : 0); i += kWarps * 32) bt_s[i] = bt_row[pg0 + i];
   if (tid == 0) {
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);
@@ -571,6 +640,28 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
       if (d == 0) p.lse_part[row] = (M + lg2(den)) * kLn2;
     }
   }
+  if (direct || p.merge_cnt == nullptr) return;
+
+  // ---- the last split of this (request, kv head group) to finish merges ----
+  // Release: every thread's partials, then (thread 0) a fence and the
+  // arrival.  The CTA whose arrival completes the count acquires them all.
+  // No CTA waits for another, and the last one resets the counter.
+  __syncthreads();
+  int* s_last = reinterpret_cast<int*>(smem);   // warp states are no longer read
+  if (tid == 0) {
+    uint32_t* cnt = p.merge_cnt + static_cast<int64_t>(b) * gridDim.y + blockIdx.y;
+    __threadfence();
+    const uint32_t prev = atomicAdd(cnt, 1u);
+    const int last = prev + 1 == static_cast<uint32_t>(r.n_splits);
+    if (last) {
+      atomicExch(cnt, 0u);
+      __threadfence();
+    }
+    *s_last = last;
+  }
+  __syncthreads();
+  if (*s_last == 0) return;
+  merge_splits<D>(p, r.n_splits, R, Gc, kvh * G + head0, qrow0);
 }
 
 // LSE merge: one warp per (query row, q head); lane owns D/32 consecutive dims.
@@ -638,9 +729,10 @@ cudaError_t launch_variant(const CUtensorMap& tmk, const CUtensorMap& tmv, const
     if (e != cudaSuccess) return e;
   }
   // with one split per request the split kernel writes the outputs itself
-  // (and flags any request that would need more): no merge launch
+  // (and flags any request that would need more), and with arrival counters
+  // the last split of each request merges: no merge launch
   const int warps = p.batch * p.q_len * p.num_q_heads;
-  if (warps > 0 && p.max_splits > 1) {
+  if (warps > 0 && p.max_splits > 1 && p.merge_cnt == nullptr) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((warps + 3) / 4);
     cfg.blockDim = dim3(128);

@@ -60,8 +60,8 @@ extern "C" pa_status pa_decode_static_scratch(
   void* scratch = nullptr;
   const pa_status st = pa::static_scratch(&scratch);
   if (st != PA_OK) return st;
-  // The kernels only OR error codes into the header, so it must start at zero;
-  // the split partials behind it are always written before they are read.
+  // The header (error word, split-arrival counters) must start at zero; the
+  // split partials behind it are always written before they are read.
   if (cudaMemsetAsync(scratch, 0, pa::kScratchHeaderBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PA_ERR_CUDA;
   return pa_decode(plan, q, q_stride_tok, q_stride_head, k_cache, v_cache, kv_stride_page, kv_stride_tok,

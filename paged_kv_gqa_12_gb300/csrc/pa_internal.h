@@ -9,8 +9,13 @@
 
 namespace pa {
 
-// Scratch header: the first 256 bytes of every scratch workspace.
-constexpr int64_t kScratchHeaderBytes = 256;
+// Scratch header at the start of every scratch workspace: the error word,
+// then (from byte 256) one split-arrival counter per (request, kv head group)
+// for decode plans whose last split merges the others.  Zero when a call
+// starts; every call leaves it zero unless it reported a device error.
+constexpr int64_t kScratchHeaderBytes = 65536;
+constexpr int64_t kMergeCounterOffset = 256;
+constexpr int64_t kMergeCounters = (kScratchHeaderBytes - kMergeCounterOffset) / 4;
 // Device error codes OR-ed into the header's first word.
 constexpr uint32_t kErrWaitTimeout = 1u;        // an mbarrier wait ran out of time
 constexpr uint32_t kErrSchedOverflow = 2u;      // extend work list exceeded its capacity
@@ -47,6 +52,8 @@ struct DecodeParams {
   int q_len;                  // query tokens per request: 1 (decode) or 1 + speculative (verify)
   int head_groups;            // CTAs per kv head: ceil(group / 16) for decode groups above 16, else 1
   const int32_t* qsl;         // verify: query_start_loc, checked to be b * q_len; null for decode
+  uint32_t* merge_cnt;        // [B, Hkv * head_groups] split-arrival counters: the last split of a
+                              // request's kv head merges its splits; null = a merge kernel follows
   uint32_t* err;              // scratch header error word
 };
 

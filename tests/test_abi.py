@@ -55,7 +55,7 @@ def test_plan_decode_defaults(lib):
     assert p.tile_tokens in (16, 32, 64)
     assert p.max_splits >= 1 and p.split_tiles >= 1
     assert p.grid[0] == p.max_splits and p.grid[1] == 8 and p.grid[2] == 64
-    assert p.scratch_bytes >= 256 + 64 * 32 * p.max_splits * (128 + 1) * 4
+    assert p.scratch_bytes >= pb.SCRATCH_HEADER_BYTES + 64 * 32 * p.max_splits * (128 + 1) * 4
     assert p.smem_bytes <= 232448
 
 
@@ -159,8 +159,9 @@ def test_plan_verify_rejects(lib, q_len, status):
 def test_plan_verify_scratch_scales_with_q_len(lib):
     one = _plan(mode=pb.MODE_VERIFY, q_len=1, max_total_q=64, num_splits=4)
     four = _plan(mode=pb.MODE_VERIFY, q_len=4, max_total_q=256, num_splits=4)
-    assert four.scratch_bytes > 3 * (one.scratch_bytes - 256)
-    assert four.launches == 2
+    h = pb.SCRATCH_HEADER_BYTES
+    assert four.scratch_bytes - h > 3 * (one.scratch_bytes - h)
+    assert four.split_merge == 1 and four.launches == 1
 
 
 def test_plan_extend_e4m3_copy_choice(lib):
@@ -180,8 +181,21 @@ def test_plan_extend_e4m3_copy_choice(lib):
 def test_plan_single_split_makes_one_launch(lib):
     # one split per request: the split kernel writes the outputs, no merge launch
     one = _plan(num_splits=1)
-    assert one.max_splits == 1 and one.launches == 1
-    assert _plan(num_splits=2).launches == 2
+    assert one.max_splits == 1 and one.launches == 1 and one.split_merge == 0
+
+
+def test_plan_split_merge_follows_counter_capacity(lib):
+    # several splits: the last split of each (request, kv head) merges while the
+    # scratch header has a counter per pair; beyond that a merge kernel follows
+    two = _plan(num_splits=2)
+    assert two.split_merge == 1 and two.launches == 1
+    fits = _plan(num_splits=2, max_batch=pb.MERGE_COUNTERS // 8)
+    assert fits.split_merge == 1 and fits.launches == 1
+    over = _plan(num_splits=2, max_batch=pb.MERGE_COUNTERS // 8 + 1)
+    assert over.split_merge == 0 and over.launches == 2
+    # head groups count: group 32 over 2 kv heads is 4 pairs per request
+    g = _plan(num_splits=2, num_q_heads=64, num_kv_heads=2, max_batch=pb.MERGE_COUNTERS // 4 + 1)
+    assert g.split_merge == 0 and g.launches == 2
 
 
 def test_plan_decode_large_group_uses_head_groups(lib):

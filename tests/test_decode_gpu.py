@@ -159,3 +159,36 @@ def test_full_size_decode_workloads_sampled(name):
     ref_o, ref_l = oracle.attention(p, rows=rows)
     gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what=wl.WORKLOADS[name])
     assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+def test_merge_paths_reuse_one_scratch():
+    # Several splits per request.  With a counter per (request, kv head) in the
+    # scratch header the split that finishes last merges (one launch); a plan
+    # whose capacity exceeds the counters launches the merge kernel.  Each
+    # plan's scratch serves three different batches in a row without being
+    # re-initialised: every call must leave its counters at zero.
+    import torch
+    from paged_kv_gqa_12_gb300 import binding as pb
+    # one plan per path, so the three batches share its window and sinks
+    batches = [[900, 3000, 17, 1], [2500, 5, 1200], [4000, 4000]]
+    probs = [wl.build_problem("decode", num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                              seq_lens=lens, window=700, sinks=True, seed=41 + i, bt_width=256)
+             for i, lens in enumerate(batches)]
+    refs = [oracle.attention(p) for p in probs]
+    for max_batch, fused in ((4, 1), (pb.MERGE_COUNTERS // 8 + 1, 0)):
+        plan = gh.make_plan(probs[0], num_splits=5, host_lens=False, max_batch=max_batch)
+        assert plan.split_merge == fused and plan.launches == 2 - fused and plan.max_splits == 5
+        scratch = pb.alloc_scratch(plan)
+        for p, (ref_o, ref_l) in zip(probs, refs):
+            d = gh.upload(p)
+            out = torch.full(p.q.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+            lse = torch.full(p.q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+            pb.decode(plan, d["q"], d["k"], d["v"], d["bt"], d["sl"], scale=p.scale, out=out, lse=lse,
+                      sinks=d["sinks"], scratch=scratch)
+            torch.cuda.synchronize()
+            assert pb.check(scratch) == 0
+            gh.assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l,
+                             what=f"max_batch={max_batch}, lens={p.seq_lens.tolist()}")
+        # the header's counters are back at zero after the last call
+        hdr = scratch[:pb.SCRATCH_HEADER_BYTES].cpu().numpy()
+        assert not hdr.any()
