@@ -192,3 +192,33 @@ def test_merge_paths_reuse_one_scratch():
         # the header's counters are back at zero after the last call
         hdr = scratch[:pb.SCRATCH_HEADER_BYTES].cpu().numpy()
         assert not hdr.any()
+
+
+def test_length_beyond_capacity_is_flagged_and_scratch_recovers():
+    # A request longer than the plan's capacity (block-table width x page
+    # size) is refused on the device before anything of it is read; the
+    # other requests of the call, split and merged by their last split, are
+    # still exact.  After pa_check the same scratch serves the next call.
+    import torch
+    from paged_kv_gqa_12_gb300 import binding as pb
+    W = 16                                                   # 256 keys per request at most
+    good = wl.build_problem("decode", num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                            seq_lens=[200, 250, 100], seed=91, bt_width=W)
+    plan = gh.make_plan(good)
+    assert plan.max_splits > 1 and plan.split_merge == 1
+    scratch = pb.alloc_scratch(plan)
+    d = gh.upload(good)
+    ref_o, ref_l = oracle.attention(good)
+    bad_lens = torch.tensor([200, 600, 100], dtype=torch.int32, device="cuda")
+    out = torch.full(good.q.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full(good.q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+    pb.decode(plan, d["q"], d["k"], d["v"], d["bt"], bad_lens, scale=good.scale, out=out, lse=lse, scratch=scratch)
+    assert pb.check(scratch) == 4                            # length beyond the plan's capacity
+    o, l = out.float().cpu().numpy(), lse.cpu().numpy()
+    for b in (0, 2):
+        gh.assert_parity(o[b:b + 1], l[b:b + 1], ref_o[b:b + 1], ref_l[b:b + 1], what=f"request {b} beside the bad one")
+    assert not scratch[:pb.SCRATCH_HEADER_BYTES].cpu().numpy().any()
+    out.fill_(float("nan"))
+    pb.decode(plan, d["q"], d["k"], d["v"], d["bt"], d["sl"], scale=good.scale, out=out, lse=lse, scratch=scratch)
+    assert pb.check(scratch) == 0
+    gh.assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, what="after recovery")
