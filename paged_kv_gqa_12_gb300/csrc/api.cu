@@ -311,7 +311,12 @@ pa_status run_split_kv(const pa_plan_t* plan, const void* q, int64_t q_stride_to
   if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale)) return PA_ERR_INVALID_ARG;
   if ((sinks != nullptr) != (s.has_sinks != 0)) return PA_ERR_INVALID_ARG;
   if (!scratch || scratch_bytes < plan->scratch_bytes) return !scratch ? PA_ERR_INVALID_ARG : PA_ERR_SCRATCH_TOO_SMALL;
+  if (scratch_bytes < kScratchHeaderBytes) return PA_ERR_SCRATCH_TOO_SMALL;
   if (!aligned(scratch, 256)) return PA_ERR_UNSUPPORTED;
+  // a plan edited by hand must not index arrival counters past the header
+  if (plan->split_merge != 0 &&
+      static_cast<int64_t>(s.max_batch) * s.num_kv_heads * split_kv_head_groups(s) > kMergeCounters)
+    return PA_ERR_INVALID_ARG;
   if (batch == 0) return PA_OK;
   if (!block_table || !seq_lens || bt_stride < 0) return PA_ERR_INVALID_ARG;
   pa_status st = check_rows(q, q_stride_tok, q_stride_head, true);

@@ -124,6 +124,18 @@ def test_decode_rejects_before_launch(lib, over, status):
     assert _decode_args(plan, **over) == status
 
 
+def test_decode_rejects_hand_edited_plans(lib):
+    # split_merge set on a plan whose pairs exceed the header's counters, or a
+    # scratch size below the header: refused before anything is enqueued
+    plan = _plan(max_batch=pb.MERGE_COUNTERS // 8 + 1, num_splits=2)
+    assert plan.split_merge == 0
+    plan.split_merge = 1
+    assert _decode_args(plan) == pb.PA_ERR_INVALID_ARG
+    small = _plan(num_splits=1)
+    small.scratch_bytes = 4096
+    assert _decode_args(small, sbytes=4096) == pb.PA_ERR_SCRATCH_TOO_SMALL
+
+
 def test_decode_empty_batch_is_noop(lib):
     plan = _plan()
     assert _decode_args(plan, batch=0) == pb.PA_OK
