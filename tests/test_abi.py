@@ -59,6 +59,16 @@ def test_plan_decode_defaults(lib):
     assert p.smem_bytes <= 232448
 
 
+def test_scratch_layout_matches_binding_constants(lib):
+    # header (error word + arrival counters), then o_part [B, Hq, S, D] and
+    # lse_part [B, Hq, S] fp32, each rounded up to 256 bytes
+    p = _plan(num_splits=3)
+    o_part = 64 * 32 * 3 * 128 * 4
+    lse_part = -(-(64 * 32 * 3 * 4) // 256) * 256
+    assert p.scratch_bytes == pb.SCRATCH_HEADER_BYTES + o_part + lse_part
+    assert pb.MERGE_COUNTERS == (pb.SCRATCH_HEADER_BYTES - 256) // 4
+
+
 def test_plan_uses_host_lengths(lib):
     short = _plan(host_seq_lens=[600] * 64)
     long = _plan(host_seq_lens=[8000] * 64)
