@@ -67,9 +67,14 @@ def test_random_case(mode, seed):
     p, kw = _draw(7000 + 97 * seed + len(mode), mode)
     ref_o, ref_l = oracle.attention(p)
     if mode == "decode":
-        for ns in (0, 2):
+        # planner, two and eleven splits (more than the eight the merge folds
+        # at once), and a capacity-only plan with room for more requests
+        for ns in (0, 2, 11):
             out, lse = gh.run(p, num_splits=ns)
             gh.assert_parity(out, lse, ref_o, ref_l, what=f"{mode} seed {seed} splits {ns}")
+        plan = gh.make_plan(p, host_lens=False, max_batch=p.batch + 3)
+        out, lse = gh.run(p, plan=plan)
+        gh.assert_parity(out, lse, ref_o, ref_l, what=f"{mode} seed {seed} capacity plan")
     else:
         out, lse = gh.run(p, **kw)
         gh.assert_parity(out, lse, ref_o, ref_l, what=f"{mode} seed {seed}")
