@@ -40,6 +40,7 @@ if ROOT not in sys.path:
 
 DECODE_WORKLOAD = "decode_llama3_8b"
 EXTEND_WORKLOAD = "prefill"
+DECODE_WORKLOADS = ("decode_llama3_8b", "decode_e4m3_window", "decode_softcap_d256", "decode_tiny")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -64,6 +65,17 @@ def decode_bytes(p) -> int:
     B, Hq, D = p.batch, p.num_q_heads, p.head_dim
     pages = int(((L + p.page_size - 1) // p.page_size).sum())
     return kv + B * Hq * D * 2 * 2 + B * Hq * 4 + pages * 4
+
+
+def decode_plan_kw(pb, p, name: str, splits: int = 0) -> dict:
+    """pa_plan arguments for a decode workload (the tiny one fixes 4 splits;
+    `splits` > 0 fixes the split count, for profiling reduced cases in the
+    launch shape of the full workload)."""
+    return dict(mode=pb.MODE_DECODE, num_q_heads=p.num_q_heads, num_kv_heads=p.num_kv_heads,
+                head_dim=p.head_dim, page_size=p.page_size,
+                kv_dtype=pb.KV_FP8_E4M3 if p.kv_dtype == "fp8_e4m3" else pb.KV_BF16, max_batch=p.batch,
+                max_pages_per_seq=p.block_table.shape[1], window=p.window, has_sinks=p.sinks is not None,
+                soft_cap=p.soft_cap, num_splits=splits if splits > 0 else (4 if name == "decode_tiny" else 0))
 
 
 def extend_flops(p) -> int:
@@ -207,14 +219,10 @@ def run_ours(args):
                     sinks=None if p.sinks is None else t(p.sinks))
 
     # Weak scaling: each rank holds its own copy of the per-GPU workload.
-    dp = wl.workload_problem(DECODE_WORKLOAD, batch=args.decode_batch)
+    dp = wl.workload_problem(args.decode_workload, batch=args.decode_batch)
     ep = wl.workload_problem(EXTEND_WORKLOAD, batch=args.extend_batch)
     dd, ed = upload(dp), upload(ep)
-    kvd = pb.KV_BF16
-    dplan_kw = dict(mode=pb.MODE_DECODE, num_q_heads=dp.num_q_heads, num_kv_heads=dp.num_kv_heads,
-                    head_dim=dp.head_dim, page_size=dp.page_size, kv_dtype=kvd, max_batch=dp.batch,
-                    max_pages_per_seq=dp.block_table.shape[1], window=dp.window,
-                    has_sinks=dp.sinks is not None, soft_cap=dp.soft_cap)
+    dplan_kw = decode_plan_kw(pb, dp, args.decode_workload, args.decode_splits)
     dplan = pb.plan(**dplan_kw, host_seq_lens=dp.seq_lens)
     dscr = pb.alloc_scratch(dplan, dev)
     dout = torch.empty(dp.q.shape, dtype=torch.bfloat16, device=dev)
@@ -322,7 +330,9 @@ def run_ours(args):
     h2d = hq.numel() * 2 + hbt.numel() * 4 + hsl.numel() * 4
     d2h = hout.numel() * 2 + hlse.numel() * 4
 
-    extras = None if args.no_extras else measure_extras(pb, wl, dp, dd, dev, stream)
+    # the extras are stated for the default decode workload's sequences
+    extras = None if args.no_extras or args.decode_workload != DECODE_WORKLOAD or args.decode_splits else \
+        measure_extras(pb, wl, dp, dd, dev, stream)
 
     if rank != 0:
         if world > 1:
@@ -338,7 +348,10 @@ def run_ours(args):
         dec_ach = dbytes / dec_mean / 1e9
         kernels["decode"] = {"bound": "hbm", "achieved": round(dec_ach, 1), "peak": hbm, "unit": "GB/s",
                              "frac": round(dec_ach / hbm, 4),
-                             "traffic": recorded_traffic("decode_split_kernel", ["decode.cu", "ptx.cuh", "pa_internal.h"]),
+                             # the record is per launch of the full default workload
+                             "traffic": recorded_traffic("decode_split_kernel", ["decode.cu", "ptx.cuh", "pa_internal.h"])
+                             if (args.decode_workload == DECODE_WORKLOAD and args.decode_batch is None
+                                 and args.decode_splits == 0) else None,
                              "timed": "pa_decode call (split kernel; the last split of each request and kv head merges), CUDA events, mean over steps",
                              "algorithmic_bytes_per_launch": dbytes, "peak_source": f"{peak_src} hbm_gbs"}
     if extend_ok:
@@ -346,7 +359,8 @@ def run_ours(args):
         ext_ach = eflops / ext_mean / 1e12
         kernels["extend"] = {"bound": "tensor", "achieved": round(ext_ach, 2), "peak": bf16, "unit": "TFLOP/s",
                              "frac": round(ext_ach / bf16, 4),
-                             "traffic": recorded_traffic("extend_attn_kernel", ["extend.cu", "ptx.cuh", "tcgen05.cuh", "pa_internal.h"]),
+                             "traffic": recorded_traffic("extend_attn_kernel", ["extend.cu", "ptx.cuh", "tcgen05.cuh", "pa_internal.h"])
+                             if args.extend_batch is None else None,
                              "timed": "pa_extend call (scheduler + attention kernel), CUDA events, mean over steps",
                              "algorithmic_flops_per_launch": eflops, "peak_source": f"{peak_src} bf16_tflops (burst)"}
     dominant = "decode" if decode_on else "extend"
@@ -370,7 +384,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; N(0,1) values, shuffled page pools)",
-        "config": {"workload": "decode " + wl.WORKLOADS[DECODE_WORKLOAD] + " + extend " + wl.WORKLOADS[EXTEND_WORKLOAD],
+        "config": {"workload": "decode " + wl.WORKLOADS[args.decode_workload] + " + extend " + wl.WORKLOADS[EXTEND_WORKLOAD],
                    "decode_batch": dp.batch, "decode_tokens": int(dp.seq_lens.sum()),
                    "extend_batch": ep.batch, "extend_q_rows": ep.num_rows,
                    "l2": "not flushed: each step streams > 1.2 GB (L2 129 MB) in a fixed order",
@@ -459,6 +473,45 @@ def measure_extras(pb, wl, dp, dd, dev, stream):
                          "tflops": round(fl / t / 1e12, 2),
                          "frac_of_bf16_peak": round(fl / t / 1e12 / float(peaks.get("bf16_tflops", 1900.0)), 4),
                          "device_error": pb.check(escr8)}
+    # the other decode workloads: each call timed alone, L2 flushed before it
+    peak_hbm = float(peaks.get("hbm_gbs", 6800.0))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for name in DECODE_WORKLOADS[1:]:
+        p = wl.workload_problem(name)
+
+        def t8(a):
+            if a.dtype == np.uint16:
+                return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        g = {k: t8(getattr(p, a)) for k, a in (("q", "q"), ("k", "k_cache"), ("v", "v_cache"),
+                                              ("bt", "block_table"), ("sl", "seq_lens"))}
+        g["sinks"] = None if p.sinks is None else t8(p.sinks)
+        plan = pb.plan(**decode_plan_kw(pb, p, name), host_seq_lens=p.seq_lens)
+        scr = pb.alloc_scratch(plan, dev)
+        out = torch.empty(p.q.shape, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(p.q.shape[:2], dtype=torch.float32, device=dev)
+
+        def call():
+            pb.decode(plan, g["q"], g["k"], g["v"], g["bt"], g["sl"], scale=p.scale, out=out, lse=lse,
+                      sinks=g["sinks"], k_scale=p.k_scale, v_scale=p.v_scale, scratch=scr, stream=stream)
+        for _ in range(5):
+            call()
+        ms = []
+        for i in range(30):
+            flush.fill_(i & 255)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        t = statistics.median(ms) / 1e3
+        nb = decode_bytes(p)
+        res[name] = {"workload": wl.WORKLOADS[name], "ms": round(t * 1e3, 4), "kv_read_tbs": round(nb / t / 1e12, 4),
+                     "frac_of_hbm": round(nb / t / 1e9 / peak_hbm, 4), "algorithmic_bytes": nb,
+                     "max_splits": int(plan.max_splits), "timing": "median of 30 calls, L2 flushed before each",
+                     "device_error": pb.check(scr)}
+        del g, scr, out, lse
     return res
 
 
@@ -531,6 +584,10 @@ def main():
     ap.add_argument("--only", choices=["decode", "extend"], default=None,
                     help="run one of the two calls per step (profiling of reduced cases)")
     ap.add_argument("--decode-batch", type=int, default=None, help="keep the first N decode requests")
+    ap.add_argument("--decode-workload", choices=DECODE_WORKLOADS, default=DECODE_WORKLOAD,
+                    help="decode workload of the step (profiling runs of the other decode workloads)")
+    ap.add_argument("--decode-splits", type=int, default=0,
+                    help="fixed KV splits per request (profiling a reduced batch in the full plan's shape)")
     ap.add_argument("--extend-batch", type=int, default=None, help="keep the first N extend requests")
     args = ap.parse_args()
     if args.warmup < 3:
