@@ -326,6 +326,31 @@ def test_window_equals_suffix_sequence(oracle_lib):
     assert np.array_equal(o, o2) and np.array_equal(l, l2)
 
 
+@pytest.mark.parametrize("cap", [0.0, 5.0])
+def test_split_and_lse_merge_reproduce_the_whole(oracle_lib, cap):
+    # Split-KV is an exact re-association: attention over keys [0, a) and over
+    # [a, L), merged by their log-sum-exps, is attention over [0, L).  The two
+    # parts come from the oracle itself, through its own definition: the first
+    # a keys are the request with seq_len a (same query, same pages), the last
+    # L - a keys are the request with window L - a.  The merge is written
+    # here in float64: M = max(lse1, lse2), w_i = exp(lse_i - M),
+    # O = (w1 O1 + w2 O2) / (w1 + w2), LSE = M + ln(w1 + w2).
+    import dataclasses
+    W = 9
+    p = _problem("decode", seed=66, B=3, Hq=8, Hkv=2, D=16, ps=4, lens=[37, 23, 41], soft_cap=cap)
+    o, l = oracle.attention(p)
+    head = dataclasses.replace(p, seq_lens=p.seq_lens - W)
+    tail = dataclasses.replace(p, window=W)
+    o1, l1 = oracle.attention(head)
+    o2, l2 = oracle.attention(tail)
+    M = np.maximum(l1, l2)
+    w1, w2 = np.exp(l1 - M), np.exp(l2 - M)
+    om = (w1[..., None] * o1 + w2[..., None] * o2) / (w1 + w2)[..., None]
+    lm = M + np.log(w1 + w2)
+    assert np.abs(om - o).max() <= 1e-12
+    assert np.abs(lm - l).max() <= 1e-12
+
+
 def test_extend_single_query_equals_decode(oracle_lib):
     e = _problem("extend", seed=71, B=3, Hq=8, Hkv=2, D=16, ps=4, lens=[5, 19, 33], qlens=[1, 1, 1],
                  window=6, sinks=True, soft_cap=4.0)
