@@ -517,21 +517,25 @@ def measure_extras(pb, wl, dp, dd, dev, stream):
 
 # ---- CPU oracle legs --------------------------------------------------------------
 
-def cpu_baseline(p, n_requests: int):
+def cpu_baseline(p, n_requests: int, min_seconds: float = 10.0):
     """The oracle, as it stands, on a bounded sample of the decode workload:
-    the first n_requests requests (all heads), on all host cores."""
+    the first n_requests requests (all heads), on all host cores, repeated
+    until about min_seconds of CPU work have been timed (at least 3 passes)."""
     import oracle
     rows = np.arange(min(n_requests, p.batch), dtype=np.int32)
     cores = os.cpu_count() or 1
     oracle.attention(p, rows=rows[:1], num_threads=cores)  # load + warm
-    t = time.perf_counter()
-    oracle.attention(p, rows=rows, num_threads=cores)
-    dt = time.perf_counter() - t
-    sub = sample_bytes(p, rows)
+    passes, dt = 0, 0.0
+    while passes < 3 or dt < min_seconds:
+        t = time.perf_counter()
+        oracle.attention(p, rows=rows, num_threads=cores)
+        dt += time.perf_counter() - t
+        passes += 1
+    sub = sample_bytes(p, rows) * passes
     return {"value": round(sub / dt / 1e12, 9), "unit": "TB/s", "cores": cores, "kind": "oracle",
             "seconds": round(dt, 3),
             "sample": f"decode requests 0..{len(rows) - 1} of the same workload (all {p.num_q_heads} heads), "
-                      f"{sub} algorithmic bytes"}
+                      f"{sub // passes} algorithmic bytes per pass, {passes} passes"}
 
 
 def sample_bytes(p, rows):
