@@ -27,6 +27,10 @@
 //     its P has completed); P (bf16) is written back
 //     over S and consumed from TMEM by O += P V (V read MN-major from shared
 //     memory); O stays in TMEM for the whole key loop.
+//   * head_dim 256 (one CTA per SM): Q also lives in TMEM, copied there by
+//     the softmax warps from its TMA staging area in the last K and V ring
+//     stages, so QK reads only K from shared memory and the rings are three
+//     stages deep.
 //   * Online softmax in the log2 domain with lazy rescaling: O and l are
 //     rescaled only when the row maximum grows by more than 2^8, which is
 //     exact because the final normalisation uses the same stale maximum.
@@ -250,7 +254,12 @@ struct ExtTraits {
   static constexpr int Q_BYTES = NCH * Q_CHUNK;
   static constexpr int KV_CHUNK = BN * 128;
   static constexpr int TILE = NCH * KV_CHUNK;        // K (or V) tile
-  static constexpr int SMEM_DATA = Q_BYTES + 2 * NST * TILE;  // Q, K ring, V ring
+  // head_dim 256 (bf16 tiles): Q is held in TMEM, so QK reads only K from
+  // shared memory; Q lands first in the last K and V stages of the rings
+  // (half its chunks in each) and is copied to TMEM before those stages are
+  // filled, which leaves room for three stages instead of two
+  static constexpr bool QT = (D == 256) && !FP8;
+  static constexpr int SMEM_DATA = (QT ? 0 : Q_BYTES) + 2 * NST * TILE;  // Q, K ring, V ring
   // fp8 cache: the e4m3 tile lands in the second half of the bf16 stage
   // buffer, rows of RB8 bytes (row r under bf16 row r's upper chunks when
   // D >= 128), and is dequantised in place
@@ -261,9 +270,12 @@ struct ExtTraits {
   // S buffers: as many as the columns left beside O hold (2 for head_dim
   // 128, 3 for 64, 4 for 256 with one CTA per SM); QK runs up to NSB - 1
   // tiles ahead of the softmax
-  static constexpr int NSB = (static_cast<int>(TMEM_COLS) - D) / BN;
-  static constexpr uint32_t TMEM_O = NSB * BN;       // S buffers, then O
-  static_assert(NSB >= 2 && NSB * BN + D <= static_cast<int>(TMEM_COLS), "TMEM plan: S buffers, O");
+  static constexpr int Q_COLS = QT ? D / 2 : 0;      // Q in TMEM: bf16 pairs
+  static constexpr int NSB = (static_cast<int>(TMEM_COLS) - D - Q_COLS) / BN;
+  static constexpr uint32_t TMEM_O = NSB * BN;       // S buffers, then O, then Q
+  static constexpr uint32_t TMEM_Q = TMEM_O + D;
+  static_assert(NSB >= 2 && NSB * BN + D + Q_COLS <= static_cast<int>(TMEM_COLS), "TMEM plan: S buffers, O, Q");
+  static_assert(!QT || (NST >= 2 && NCH % 2 == 0 && (NCH / 2) * Q_CHUNK <= TILE), "Q staged in the last stages");
   // S buffer of tile j and the phase parity of its barriers (unsigned: a
   // power-of-two count reduces to a mask and a shift)
   __device__ static __forceinline__ int sbuf(int j) {
@@ -272,8 +284,9 @@ struct ExtTraits {
   __device__ static __forceinline__ uint32_t sphase(int j) {
     return (static_cast<unsigned>(j) / static_cast<unsigned>(NSB)) & 1u;
   }
-  // mbarriers: q_full, six per ring stage, s_full/p_full/o_done per S buffer; then the TMEM address
-  static constexpr int BAR_BYTES = ((1 + 6 * NST + 3 * NSB) * 8 + 4 + 15) / 16 * 16;
+  // mbarriers: q_full, six per ring stage, s_full/p_full/o_done per S
+  // buffer, q_moved (Q in TMEM); then the TMEM address
+  static constexpr int BAR_BYTES = ((1 + 6 * NST + 3 * NSB + (QT ? 1 : 0)) * 8 + 4 + 15) / 16 * 16;
   static constexpr int SMEM = 1024 + SMEM_DATA + BAR_BYTES;   // 1024: alignment slack for SW128
   static_assert(CPS * SMEM <= 232448, "shared memory for CPS CTAs per SM");
   static_assert(BN % 64 == 0, "P is stored 32 columns (64 keys) at a time");
@@ -362,9 +375,19 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_s = smem;
-  uint8_t* k_s = smem + T::Q_BYTES;
+  uint8_t* k_s = smem + (T::QT ? 0 : T::Q_BYTES);
   uint8_t* v_s = k_s + NST * T::TILE;
+  // Q chunk c (64 dims of the 128 rows): its own area, or (Q in TMEM) the
+  // last K stage for the first half of the chunks and the last V stage for
+  // the second
+  auto q_chunk = [&](int c) -> uint8_t* {
+    if constexpr (T::QT) {
+      return c < T::NCH / 2 ? k_s + (NST - 1) * T::TILE + c * T::Q_CHUNK
+                            : v_s + (NST - 1) * T::TILE + (c - T::NCH / 2) * T::Q_CHUNK;
+    } else {
+      return smem + c * T::Q_CHUNK;
+    }
+  };
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::SMEM_DATA);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
@@ -376,7 +399,8 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   uint64_t* s_full = v_land + NST;
   uint64_t* p_full = s_full + T::NSB;
   uint64_t* o_done = p_full + T::NSB;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_done + T::NSB);
+  uint64_t* q_moved = o_done + T::NSB;   // Q in TMEM: the softmax warps copied it (4 arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_moved + (T::QT ? 1 : 0));
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -398,6 +422,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       mbar_init(&p_full[i], 4);
       mbar_init(&o_done[i], 1);
     }
+    if (T::QT) mbar_init(q_moved, 4);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -417,7 +442,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     if (is_k && lane == 0) {
       mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(T::NCH * p.tm * G * 128));
 #pragma unroll
-      for (int c = 0; c < T::NCH; ++c) tma_load_3d(q_s + c * T::Q_CHUNK, &tmq, c * 64, kvh * G, qs + t0, q_full);
+      for (int c = 0; c < T::NCH; ++c) tma_load_3d(q_chunk(c), &tmq, c * 64, kvh * G, qs + t0, q_full);
     }
     const int npg = BN >> ps_log2;
     // page coordinate of this lane's page of key tile j; pages with no
@@ -431,6 +456,13 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       for (int j = 0; j < n && ok; ++j) {
         const int stage = j % NST;
         if (j >= NST) ok = __all_sync(0xffffffffu, wait_or_abort(&empty[stage], ((j / NST) - 1) & 1, p.err));
+        if constexpr (T::QT) {
+          // the last stage holds Q until the softmax warps have copied it to TMEM
+          if (j == NST - 1) {
+            ok = ok && __all_sync(0xffffffffu, wait_or_abort(q_moved, 0, p.err));
+            fence_proxy_async_smem();
+          }
+        }
         if (!ok) break;
         if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(T::TILE));
         __syncwarp();
@@ -480,9 +512,9 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     // ---------------- S = Q K^T issuer (one thread) ----------------
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(kRows, BN, false, false);
-      const uint32_t q_u = smem_u32(q_s);
+      const uint32_t q_u = smem_u32(q_chunk(0));   // Q chunks in their own area (not used with Q in TMEM)
       const uint32_t k_ring = smem_u32(k_s);
-      bool ok = wait_or_abort(q_full, 0, p.err);
+      bool ok = T::QT ? wait_or_abort(q_moved, 0, p.err) : wait_or_abort(q_full, 0, p.err);
       tc_fence_after();
       for (int j = 0; j < n && ok; ++j) {
         const int stage = j % NST;
@@ -495,9 +527,14 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         const uint32_t k_u = k_ring + stage * T::TILE;
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
-          const uint64_t ad = sdesc_sw128(q_u + (s >> 2) * T::Q_CHUNK + (s & 3) * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(k_u + (s >> 2) * T::KV_CHUNK + (s & 3) * 32, 16, 1024);
-          umma_ss(tS, ad, bd, idesc_qk, s > 0 ? 1u : 0u);
+          if constexpr (T::QT) {
+            // A = Q from TMEM: k-step s is 16 dims, 8 columns
+            umma_ts(tS, tbase + T::TMEM_Q + static_cast<uint32_t>(s * 8), bd, idesc_qk, s > 0 ? 1u : 0u);
+          } else {
+            const uint64_t ad = sdesc_sw128(q_u + (s >> 2) * T::Q_CHUNK + (s & 3) * 32, 16, 1024);
+            umma_ss(tS, ad, bd, idesc_qk, s > 0 ? 1u : 0u);
+          }
         }
         umma_commit(&s_full[T::sbuf(j)]);
         umma_commit(&k_empty[stage]);
@@ -557,7 +594,33 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     const int l_pad = ((L + ps - 1) >> ps_log2) << ps_log2;   // end of the last page
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
+    if constexpr (T::QT) {
+      // Q row r (= TMEM lane r) from its staging chunks into TMEM columns
+      // TMEM_Q + 32c .. + 31 (dims 64c + 2w, 64c + 2w + 1 in column w); the
+      // 16-byte units of a 128-byte row are XOR-swizzled by (row & 7)
+      ok = __all_sync(0xffffffffu, wait_or_abort(q_full, 0, p.err));
+      if (ok) {
+#pragma unroll 1
+        for (int c = 0; c < T::NCH; ++c) {
+          const uint8_t* row = q_chunk(c) + r * 128;
+          uint32_t u[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint4 w = *reinterpret_cast<const uint4*>(row + ((k ^ (r & 7)) << 4));
+            u[4 * k] = w.x;
+            u[4 * k + 1] = w.y;
+            u[4 * k + 2] = w.z;
+            u[4 * k + 3] = w.w;
+          }
+          tmem_st32(tbase + lane_off + T::TMEM_Q + static_cast<uint32_t>(c * 32), u);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_moved);
+      }
+    }
+    for (int j = 0; j < n && ok; ++j) {
       const int k0 = (kt0 + j) * BN;
       ok = __all_sync(0xffffffffu, wait_or_abort(&s_full[T::sbuf(j)], T::sphase(j), p.err));
       if (!ok) break;
@@ -856,7 +919,7 @@ struct ExtChoice {
 ExtChoice ext_choice(int D) {
   if (D == 64) return {64, 4, ExtTraits<64, 64, 4, 2>::SMEM};
   if (D == 128) return {64, 2, ExtTraits<128, 64, 2, 2>::SMEM};
-  return {64, 2, ExtTraits<256, 64, 2, 1>::SMEM};
+  return {64, 3, ExtTraits<256, 64, 3, 1>::SMEM};   // Q in TMEM, three stages
 }
 
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -1059,7 +1122,7 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
     case 129: e = launch_ext<64, 64, 4, 2, true>(tmq, tmk, tmv, p, strm); break;
     case 256: e = launch_ext<128, 64, 2, 2, false>(tmq, tmk, tmv, p, strm); break;
     case 257: e = launch_ext<128, 64, 2, 2, true>(tmq, tmk, tmv, p, strm); break;
-    case 512: e = launch_ext<256, 64, 2, 1, false>(tmq, tmk, tmv, p, strm); break;
+    case 512: e = launch_ext<256, 64, 3, 1, false>(tmq, tmk, tmv, p, strm); break;
     default: e = launch_ext<256, 64, 2, 1, true>(tmq, tmk, tmv, p, strm); break;
   }
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;

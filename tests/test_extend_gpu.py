@@ -37,6 +37,8 @@ VARIANTS = [
     (32, 8, 128, 16),
     (8, 2, 64, 16),
     (16, 8, 256, 32),
+    (12, 4, 256, 16),     # head_dim 256, group 3: 126 of 128 rows used
+    (32, 2, 256, 64),     # head_dim 256, group 16
     (64, 8, 128, 64),     # group 8
     (16, 1, 128, 16),     # group 16
     (8, 8, 64, 32),       # group 1
