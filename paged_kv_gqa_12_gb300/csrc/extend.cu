@@ -27,10 +27,10 @@
 //     its P has completed); P (bf16) is written back
 //     over S and consumed from TMEM by O += P V (V read MN-major from shared
 //     memory); O stays in TMEM for the whole key loop.
-//   * head_dim 256 (one CTA per SM): Q also lives in TMEM, copied there by
-//     the softmax warps from its TMA staging area in the last K and V ring
-//     stages, so QK reads only K from shared memory and the rings are three
-//     stages deep.
+//   * head_dim 256 (one CTA per SM): the first half of Q's dims also lives
+//     in TMEM, copied there by the softmax warps from its TMA staging area in
+//     the last K ring stage, so half of QK's K steps read only K from shared
+//     memory; the rings are three stages deep and three S buffers fit.
 //   * Online softmax in the log2 domain with lazy rescaling: O and l are
 //     rescaled only when the row maximum grows by more than 2^8, which is
 //     exact because the final normalisation uses the same stale maximum.
@@ -254,12 +254,14 @@ struct ExtTraits {
   static constexpr int Q_BYTES = NCH * Q_CHUNK;
   static constexpr int KV_CHUNK = BN * 128;
   static constexpr int TILE = NCH * KV_CHUNK;        // K (or V) tile
-  // head_dim 256 (bf16 tiles): Q is held in TMEM, so QK reads only K from
-  // shared memory; Q lands first in the last K and V stages of the rings
-  // (half its chunks in each) and is copied to TMEM before those stages are
-  // filled, which leaves room for three stages instead of two
+  // head_dim 256 (bf16 tiles): the first half of Q's dims is held in TMEM,
+  // so half of QK's K steps read only K from shared memory; that half lands
+  // first in the last K stage of the ring and is copied to TMEM before the
+  // stage is filled, the other half keeps its own area.  This leaves room
+  // for three ring stages and three S buffers
   static constexpr bool QT = (D == 256) && !FP8;
-  static constexpr int SMEM_DATA = (QT ? 0 : Q_BYTES) + 2 * NST * TILE;  // Q, K ring, V ring
+  static constexpr int Q_TM_CH = QT ? NCH / 2 : 0;   // Q chunks held in TMEM
+  static constexpr int SMEM_DATA = (NCH - Q_TM_CH) * Q_CHUNK + 2 * NST * TILE;  // Q, K ring, V ring
   // fp8 cache: the e4m3 tile lands in the second half of the bf16 stage
   // buffer, rows of RB8 bytes (row r under bf16 row r's upper chunks when
   // D >= 128), and is dequantised in place
@@ -270,12 +272,12 @@ struct ExtTraits {
   // S buffers: as many as the columns left beside O hold (2 for head_dim
   // 128, 3 for 64, 4 for 256 with one CTA per SM); QK runs up to NSB - 1
   // tiles ahead of the softmax
-  static constexpr int Q_COLS = QT ? D / 2 : 0;      // Q in TMEM: bf16 pairs
+  static constexpr int Q_COLS = Q_TM_CH * 32;       // Q in TMEM: bf16 pairs, 32 columns per chunk
   static constexpr int NSB = (static_cast<int>(TMEM_COLS) - D - Q_COLS) / BN;
   static constexpr uint32_t TMEM_O = NSB * BN;       // S buffers, then O, then Q
   static constexpr uint32_t TMEM_Q = TMEM_O + D;
   static_assert(NSB >= 2 && NSB * BN + D + Q_COLS <= static_cast<int>(TMEM_COLS), "TMEM plan: S buffers, O, Q");
-  static_assert(!QT || (NST >= 2 && NCH % 2 == 0 && (NCH / 2) * Q_CHUNK <= TILE), "Q staged in the last stages");
+  static_assert(!QT || (NST >= 2 && Q_TM_CH * Q_CHUNK <= TILE), "Q staged in the last K stage");
   // S buffer of tile j and the phase parity of its barriers (unsigned: a
   // power-of-two count reduces to a mask and a shift)
   __device__ static __forceinline__ int sbuf(int j) {
@@ -375,18 +377,13 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* k_s = smem + (T::QT ? 0 : T::Q_BYTES);
+  uint8_t* k_s = smem + (T::NCH - T::Q_TM_CH) * T::Q_CHUNK;
   uint8_t* v_s = k_s + NST * T::TILE;
-  // Q chunk c (64 dims of the 128 rows): its own area, or (Q in TMEM) the
-  // last K stage for the first half of the chunks and the last V stage for
-  // the second
+  // Q chunk c (64 dims of the 128 rows): the chunks held in TMEM are staged
+  // in the last K stage, the others have their own area
   auto q_chunk = [&](int c) -> uint8_t* {
-    if constexpr (T::QT) {
-      return c < T::NCH / 2 ? k_s + (NST - 1) * T::TILE + c * T::Q_CHUNK
-                            : v_s + (NST - 1) * T::TILE + (c - T::NCH / 2) * T::Q_CHUNK;
-    } else {
-      return smem + c * T::Q_CHUNK;
-    }
+    return c < T::Q_TM_CH ? k_s + (NST - 1) * T::TILE + c * T::Q_CHUNK
+                          : smem + (c - T::Q_TM_CH) * T::Q_CHUNK;
   };
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::SMEM_DATA);
   uint64_t* q_full = bars;
@@ -457,8 +454,9 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         const int stage = j % NST;
         if (j >= NST) ok = __all_sync(0xffffffffu, wait_or_abort(&empty[stage], ((j / NST) - 1) & 1, p.err));
         if constexpr (T::QT) {
-          // the last stage holds Q until the softmax warps have copied it to TMEM
-          if (j == NST - 1) {
+          // the last K stage holds Q's first chunks until the softmax warps
+          // have copied them to TMEM
+          if (is_k && j == NST - 1) {
             ok = ok && __all_sync(0xffffffffu, wait_or_abort(q_moved, 0, p.err));
             fence_proxy_async_smem();
           }
@@ -512,9 +510,10 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     // ---------------- S = Q K^T issuer (one thread) ----------------
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(kRows, BN, false, false);
-      const uint32_t q_u = smem_u32(q_chunk(0));   // Q chunks in their own area (not used with Q in TMEM)
+      const uint32_t q_u = smem_u32(q_chunk(T::Q_TM_CH));   // first Q chunk in its own area
       const uint32_t k_ring = smem_u32(k_s);
-      bool ok = T::QT ? wait_or_abort(q_moved, 0, p.err) : wait_or_abort(q_full, 0, p.err);
+      bool ok = wait_or_abort(q_full, 0, p.err);
+      if (T::QT) ok = ok && wait_or_abort(q_moved, 0, p.err);
       tc_fence_after();
       for (int j = 0; j < n && ok; ++j) {
         const int stage = j % NST;
@@ -528,11 +527,11 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
 #pragma unroll
         for (int s = 0; s < D / 16; ++s) {
           const uint64_t bd = sdesc_sw128(k_u + (s >> 2) * T::KV_CHUNK + (s & 3) * 32, 16, 1024);
-          if constexpr (T::QT) {
+          if (s < T::Q_TM_CH * 4) {
             // A = Q from TMEM: k-step s is 16 dims, 8 columns
             umma_ts(tS, tbase + T::TMEM_Q + static_cast<uint32_t>(s * 8), bd, idesc_qk, s > 0 ? 1u : 0u);
           } else {
-            const uint64_t ad = sdesc_sw128(q_u + (s >> 2) * T::Q_CHUNK + (s & 3) * 32, 16, 1024);
+            const uint64_t ad = sdesc_sw128(q_u + ((s >> 2) - T::Q_TM_CH) * T::Q_CHUNK + (s & 3) * 32, 16, 1024);
             umma_ss(tS, ad, bd, idesc_qk, s > 0 ? 1u : 0u);
           }
         }
@@ -601,7 +600,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       ok = __all_sync(0xffffffffu, wait_or_abort(q_full, 0, p.err));
       if (ok) {
 #pragma unroll 1
-        for (int c = 0; c < T::NCH; ++c) {
+        for (int c = 0; c < T::Q_TM_CH; ++c) {
           const uint8_t* row = q_chunk(c) + r * 128;
           uint32_t u[32];
 #pragma unroll
