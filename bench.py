@@ -57,13 +57,15 @@ def load_peaks():
 # ---- algorithmic work (per call) -------------------------------------------------
 
 def decode_bytes(p) -> int:
-    """K+V of the attended keys + q + out + lse + block-table entries read."""
+    """K+V of the attended keys + q + out + lse + the block-table entries of
+    the pages those keys span (a window starting inside a page spans it)."""
     e = 1 if p.kv_dtype == "fp8_e4m3" else 2
     L = p.seq_lens.astype(np.int64)
     n = np.minimum(L, p.window) if p.window > 0 else L
     kv = int(n.sum()) * p.num_kv_heads * p.head_dim * e * 2
     B, Hq, D = p.batch, p.num_q_heads, p.head_dim
-    pages = int(((L + p.page_size - 1) // p.page_size).sum())
+    ps = p.page_size
+    pages = int(np.where(n > 0, (L - 1) // ps - (L - n) // ps + 1, 0).sum())
     return kv + B * Hq * D * 2 * 2 + B * Hq * 4 + pages * 4
 
 
