@@ -415,6 +415,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
           mx[j][e & 1] = fmaxf(mx[j][e & 1], v);
         }
     float alpha[NH8][2], mu[NH8][2];
+    bool grew = false;   // some row's running maximum rose (else every alpha is ex2(0) = 1)
 #pragma unroll
     for (int j = 0; j < NH8; ++j)
 #pragma unroll
@@ -425,10 +426,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
         const float m_new = fmaxf(m_run[j][h], m);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        grew |= m_new > m_run[j][h];
         alpha[j][h] = ex2(m_run[j][h] - m_use);
         m_run[j][h] = m_new;
         mu[j][h] = m_use;
       }
+    // the accumulators need rescaling only after a maximum rose somewhere in
+    // the warp; multiplying by exactly 1 is skipped
+    const bool rescale = __any_sync(0xffffffffu, grew);
 #pragma unroll
     for (int j = 0; j < NH8; ++j) {
       float ls0 = 0.f, ls1 = 0.f;
@@ -443,12 +448,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
       }
       l_run[j][0] = l_run[j][0] * alpha[j][0] + ls0;
       l_run[j][1] = l_run[j][1] * alpha[j][1] + ls1;
+      if (rescale) {
 #pragma unroll
-      for (int i = 0; i < T::KS; ++i) {
-        o[i][j][0] *= alpha[j][0];
-        o[i][j][1] *= alpha[j][1];
-        o[i][j][2] *= alpha[j][0];
-        o[i][j][3] *= alpha[j][1];
+        for (int i = 0; i < T::KS; ++i) {
+          o[i][j][0] *= alpha[j][0];
+          o[i][j][1] *= alpha[j][1];
+          o[i][j][2] *= alpha[j][0];
+          o[i][j][3] *= alpha[j][1];
+        }
       }
     }
 
