@@ -24,8 +24,9 @@
 //     P^T is formed in registers with movmatrix.
 //   * fp8-e4m3 K/V are dequantised in registers to bf16 exactly as the
 //     prefix-prefill page does: bf16(float(code) * scale).
-//   * Online softmax in the log2 domain; per-thread partial row sums are
-//     reduced once at the end; the 4 warps' states are merged in shared
+//   * Online softmax in the log2 domain (accumulators rescaled only on tiles
+//     where a row maximum rose); per-thread partial row sums are reduced
+//     once at the end; the 4 warps' states are merged in shared
 //     memory.  A request with one split writes the final output directly;
 //     otherwise each split writes its normalised partial and LSE, and the
 //     split that finishes last for its (request, kv head) -- counted by an
