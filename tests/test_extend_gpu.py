@@ -115,6 +115,22 @@ def test_extend_full_size_workload_sampled():
     gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what="extend workload, full size")
 
 
+def test_extend_e4m3_full_size_workload_sampled():
+    # the benchmark's e4m3 extend measurement at full size (scales 0.05, the
+    # dequantised bf16 copy the plan chooses), on sampled rows
+    p = wl.workload_problem("prefill", kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05)
+    assert gh.make_plan(p).kv_copy == 1
+    out, lse = gh.run(p)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    rng = np.random.default_rng(8)
+    qsl = p.query_start_loc
+    rows = [int(qsl[b]) for b in range(p.batch)] + [int(qsl[b + 1]) - 1 for b in range(p.batch)]
+    rows += list(rng.choice(p.num_rows, size=40, replace=False))
+    rows = np.unique(np.array(rows, np.int32))
+    ref_o, ref_l = oracle.attention(p, rows=rows)
+    gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what="e4m3 extend workload, full size")
+
+
 FP8_VARIANTS = [(32, 8, 128, 16), (8, 2, 64, 16), (16, 8, 256, 32), (64, 8, 64, 64)]
 
 

@@ -89,3 +89,24 @@ def test_verify_rejects_unequal_packing():
     with pytest.raises(pb.PaError):
         pb.extend(plan, d3["q"], d3["k"], d3["v"], d3["bt"], d3["sl"], d3["qsl"], scale=q3.scale, out=out3,
                   scratch=scratch)
+
+
+def test_verify_full_size_sampled():
+    # The benchmark's verify measurement at full size, in its launch
+    # configuration: the Llama-3-8B-shaped decode workload's cache and
+    # lengths, 4 new query tokens per request (their K/V already in the
+    # pages), a verify plan from host lengths; the oracle evaluates a sample
+    # of rows, among them the first and last row of every request.
+    import dataclasses
+    dp = wl.workload_problem("decode_llama3_8b")
+    q_len = 4
+    rng = np.random.default_rng(77)
+    q = wl._to_bf16_bits(rng.standard_normal((dp.batch * q_len, dp.num_q_heads, dp.head_dim), dtype=np.float32))
+    p = dataclasses.replace(dp, mode="extend", q=q,
+                            query_start_loc=np.arange(0, dp.batch * q_len + 1, q_len, dtype=np.int32))
+    out, lse = gh.run(p, verify=True)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    rows = [b * q_len for b in range(dp.batch)] + [b * q_len + q_len - 1 for b in range(dp.batch)]
+    rows = np.unique(np.array(rows + list(rng.choice(p.num_rows, size=32, replace=False)), np.int32))
+    ref_o, ref_l = oracle.attention(p, rows=rows)
+    gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what="verify, decode workload, full size")
