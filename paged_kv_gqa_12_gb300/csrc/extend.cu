@@ -204,11 +204,16 @@ __device__ __forceinline__ float tanh_exp2(float x) {
 }
 
 // A key tile in which some query row of the item masks some key (causal
-// diagonal, window edge or sequence end).  There the softmax weights are
-// passed as P = P_hi + P_lo (two bf16 halves, two PV MMAs): rows with only a
-// few attended keys live in such tiles, and one bf16 P (2^-9 relative) is not
-// averaged out over few keys.  Elsewhere every row attends to the whole tile.
-__device__ __forceinline__ bool split_p_tile(int k0, int bn, int pos_min, int lo_max, int L) {
+// diagonal, window edge or sequence end), in an item where some row attends
+// fewer than kExactKeys keys in all.  There the softmax weights are passed as
+// P = P_hi + P_lo (two bf16 halves, two PV MMAs): one bf16 P (2^-9 relative)
+// is not averaged out over a few keys.  Rows of an item whose first row
+// already attends kExactKeys keys (min(position + 1, window) of them) take
+// one bf16 P on every tile, as they do on their unmasked tiles.
+constexpr int kExactKeys = 128;
+__device__ __forceinline__ bool split_p_tile(int k0, int bn, int pos_min, int lo_max, int L, int window) {
+  const int min_keys = window > 0 ? min(pos_min + 1, window) : pos_min + 1;
+  if (min_keys >= kExactKeys) return false;
   return !(k0 >= lo_max && k0 + bn - 1 <= pos_min && k0 + bn <= L);
 }
 
@@ -557,7 +562,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         const uint32_t v_u = v_ring + st * T::TILE;
         // P columns: k-step s (16 keys) at column 8s; on split tiles P_hi at
         // 16s and P_lo at 16s + 8
-        const bool split = split_p_tile((kt0 + jj) * BN, BN, pos_min, lo_max, L);
+        const bool split = split_p_tile((kt0 + jj) * BN, BN, pos_min, lo_max, L, p.window);
         const uint32_t pstep = split ? 16u : 8u;
 #pragma unroll
         for (int s = 0; s < BN / 16; ++s) {
@@ -630,7 +635,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       tmem_wait_ld();
       const bool full = (k0 >= lo) && (k0 + BN - 1 <= pos);
-      const bool split = split_p_tile(k0, BN, ctx + t0, lo_max_cta, L);
+      const bool split = split_p_tile(k0, BN, ctx + t0, lo_max_cta, L, p.window);
       float mx8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
