@@ -72,3 +72,32 @@ def test_c_program_links_against_the_library(cc, tmp_path):
     r = subprocess.run([cc, "-std=c11", "-I" + os.path.join(ROOT, "include"), str(src), lib,
                         "-Wl,-rpath," + os.path.dirname(lib), "-o", str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_binding_struct_layouts_match_the_header(cc, tmp_path):
+    # the ctypes mirrors of pa_shape and pa_plan_t: size and every field offset
+    # as the C compiler lays them out
+    import ctypes
+    from paged_kv_gqa_12_gb300 import binding as pb
+    fields = {"pa_shape": [f[0] for f in pb.PaShape._fields_],
+              "pa_plan_t": [f[0] for f in pb.PaPlan._fields_]}
+    lines = ["#include <stddef.h>", "#include <stdio.h>", "#include \"pa.h\"", "int main(void) {"]
+    for st, names in fields.items():
+        lines.append(f'  printf("{st} size %zu\\n", sizeof({st}));')
+        for n in names:
+            lines.append(f'  printf("{st} {n} %zu\\n", offsetof({st}, {n}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    r = subprocess.run([cc, "-std=c11", "-I" + os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    got = {}
+    for line in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines():
+        parts = line.split()
+        got[(parts[0], parts[1])] = int(parts[2])
+    for st, cls in (("pa_shape", pb.PaShape), ("pa_plan_t", pb.PaPlan)):
+        assert got[(st, "size")] == ctypes.sizeof(cls), st
+        for n in fields[st]:
+            assert got[(st, n)] == getattr(cls, n).offset, (st, n)
