@@ -54,7 +54,7 @@ def test_verify_per_request_scales():
     gh.assert_parity(out, lse, ref_o, ref_l, what="verify per-request scales")
 
 
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 def test_extend_per_request_scales_both_paths(D):
     from paged_kv_gqa_12_gb300 import binding as pb
     ctx = np.array([0, 5, 300, 1000, 129])
