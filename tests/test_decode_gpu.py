@@ -147,18 +147,16 @@ def test_no_lse_output():
 
 
 @pytest.mark.parametrize("name", ["decode_llama3_8b", "decode_e4m3_window", "decode_softcap_d256"])
-def test_full_size_decode_workloads_sampled(name):
+def test_full_size_decode_workloads_all_rows(name):
     # The benchmark workloads at full size, in the launch configuration the
-    # benchmark uses (planner with host lengths); the oracle evaluates a
-    # sample of rows one by one.
+    # benchmark uses (planner with host lengths); every output element and
+    # every LSE of every request and head is compared with the oracle.
     p = wl.workload_problem(name)
     out, lse = gh.run(p)
-    rng = np.random.default_rng(len(name))
-    rows = np.unique(np.concatenate([rng.choice(p.batch, size=12, replace=False),
-                                     [int(np.argmax(p.seq_lens)), int(np.argmin(p.seq_lens))]])).astype(np.int32)
-    ref_o, ref_l = oracle.attention(p, rows=rows)
-    gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what=wl.WORKLOADS[name])
     assert np.isfinite(out).all() and np.isfinite(lse).all()
+    ref_o, ref_l = oracle.attention(p)
+    eo, el = gh.assert_parity(out, lse, ref_o, ref_l, what=wl.WORKLOADS[name])
+    print(f"{name}: all {out.shape[0] * out.shape[1]} rows, max |out err| {eo:.3e}, max |lse err| {el:.3e}")
 
 
 def test_merge_paths_reuse_one_scratch():

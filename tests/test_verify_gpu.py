@@ -91,12 +91,11 @@ def test_verify_rejects_unequal_packing():
                   scratch=scratch)
 
 
-def test_verify_full_size_sampled():
+def test_verify_full_size_all_rows():
     # The benchmark's verify measurement at full size, in its launch
     # configuration: the Llama-3-8B-shaped decode workload's cache and
     # lengths, 4 new query tokens per request (their K/V already in the
-    # pages), a verify plan from host lengths; the oracle evaluates a sample
-    # of rows, among them the first and last row of every request.
+    # pages), a verify plan from host lengths; every row against the oracle.
     import dataclasses
     dp = wl.workload_problem("decode_llama3_8b")
     q_len = 4
@@ -106,7 +105,6 @@ def test_verify_full_size_sampled():
                             query_start_loc=np.arange(0, dp.batch * q_len + 1, q_len, dtype=np.int32))
     out, lse = gh.run(p, verify=True)
     assert np.isfinite(out).all() and np.isfinite(lse).all()
-    rows = [b * q_len for b in range(dp.batch)] + [b * q_len + q_len - 1 for b in range(dp.batch)]
-    rows = np.unique(np.array(rows + list(rng.choice(p.num_rows, size=32, replace=False)), np.int32))
-    ref_o, ref_l = oracle.attention(p, rows=rows)
-    gh.assert_parity(out[rows], lse[rows], ref_o, ref_l, what="verify, decode workload, full size")
+    ref_o, ref_l = oracle.attention(p)
+    eo, el = gh.assert_parity(out, lse, ref_o, ref_l, what="verify, decode workload, full size")
+    print(f"verify q_len 4: all {p.num_rows} rows, max |out err| {eo:.3e}, max |lse err| {el:.3e}")
