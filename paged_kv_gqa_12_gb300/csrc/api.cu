@@ -73,6 +73,14 @@ int split_kv_head_groups(const pa_shape& s) {
   return (s.mode == PA_MODE_DECODE && G > 16) ? (G + 15) / 16 : 1;
 }
 
+// Scratch bytes a split-KV plan needs: the header, then the normalised split
+// outputs o_part [max_batch, q_len, Hq, max_splits, D] and their LSEs, each
+// region 256-byte aligned.
+int64_t split_kv_scratch_bytes(const pa_shape& s, int64_t max_splits) {
+  const int64_t prow = static_cast<int64_t>(s.max_batch) * split_kv_qlen(s) * s.num_q_heads * max_splits;
+  return kScratchHeaderBytes + align_up(prow * s.head_dim * 4, 256) + align_up(prow * 4, 256);
+}
+
 namespace {
 
 // Keys a split-KV request attends to (union over its q_len queries): the
@@ -146,8 +154,7 @@ pa_status plan_decode(const pa_shape& s, const int32_t* host_lens, int32_t batch
   out->grid[0] = static_cast<int32_t>(max_splits);
   out->grid[1] = s.num_kv_heads * hgroups;
   out->grid[2] = s.max_batch;
-  const int64_t prow = static_cast<int64_t>(s.max_batch) * qlen * s.num_q_heads * max_splits;
-  out->scratch_bytes = kScratchHeaderBytes + align_up(prow * s.head_dim * 4, 256) + align_up(prow * 4, 256);
+  out->scratch_bytes = split_kv_scratch_bytes(s, max_splits);
   // several splits: the last split of each (request, kv head group) merges
   // them while the header has a counter for every such pair, else a merge
   // kernel follows the split kernel
@@ -313,9 +320,14 @@ pa_status run_split_kv(const pa_plan_t* plan, const void* q, int64_t q_stride_to
   if (!scratch || scratch_bytes < plan->scratch_bytes) return !scratch ? PA_ERR_INVALID_ARG : PA_ERR_SCRATCH_TOO_SMALL;
   if (scratch_bytes < kScratchHeaderBytes) return PA_ERR_SCRATCH_TOO_SMALL;
   if (!aligned(scratch, 256)) return PA_ERR_UNSUPPORTED;
-  // a plan edited by hand must not index arrival counters past the header
+  // a plan edited by hand must not index arrival counters past the header,
+  // nor lay split partials out past the scratch_bytes it states, nor run a
+  // tile size the kernels were not compiled for
   if (plan->split_merge != 0 &&
       static_cast<int64_t>(s.max_batch) * s.num_kv_heads * split_kv_head_groups(s) > kMergeCounters)
+    return PA_ERR_INVALID_ARG;
+  if (plan->max_splits < 1 || plan->split_tiles < 0 || plan->bt_cache < 1 ||
+      plan->scratch_bytes < split_kv_scratch_bytes(s, plan->max_splits))
     return PA_ERR_INVALID_ARG;
   if (batch == 0) return PA_OK;
   if (!block_table || !seq_lens || bt_stride < 0) return PA_ERR_INVALID_ARG;
@@ -331,6 +343,7 @@ pa_status run_split_kv(const pa_plan_t* plan, const void* q, int64_t q_stride_to
   const int qlen = split_kv_qlen(s);
   const int hgroups = split_kv_head_groups(s);
   const DecodeConfig cfg = decode_config(s.head_dim, fp8, hgroups > 1 ? 16 : G * qlen, plan->bt_cache);
+  if (plan->tile_tokens != cfg.tile_tokens || cfg.smem_bytes > kMaxSmemPerCta) return PA_ERR_INVALID_ARG;
   const int box_rows = std::min(s.page_size, plan->tile_tokens);
   CUtensorMap tmk, tmv;
   if ((st = make_kv_map(&tmk, k_cache, fp8, s.head_dim, s.num_kv_heads, s.page_size, num_pages, kv_stride_page,
@@ -352,6 +365,7 @@ pa_status run_split_kv(const pa_plan_t* plan, const void* q, int64_t q_stride_to
   p.num_kv_heads = s.num_kv_heads;
   p.group = G;
   p.page_size = s.page_size;
+  p.num_pages = num_pages;
   p.scale_log2 = scale * kLog2eHost;
   p.cap_log2 = s.soft_cap > 0.f ? s.soft_cap * kLog2eHost : 0.f;
   p.scale_over_cap = s.soft_cap > 0.f ? scale / s.soft_cap : 0.f;

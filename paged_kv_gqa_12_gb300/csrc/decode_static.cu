@@ -30,18 +30,24 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBy
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_decode_scratch on the current device, looked up once per
-// device.  In host code the array's name is only a host-side handle, so the
-// address must come from the runtime.
-pa_status static_scratch(void** out) {
+// Device address of g_decode_scratch on the current device.  In host code the
+// array's name is only a host-side handle, so the address must come from the
+// runtime.  It is looked up again on every call made outside a stream capture
+// (a device reset reloads the library's module, possibly elsewhere); a call
+// being captured uses the address found by the last uncaptured call on that
+// device, and fails if there was none.
+pa_status static_scratch(cudaStream_t stream, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return PA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
     g_scratch_ptr[dev] = p;
   }
+  if (!g_scratch_ptr[dev]) return PA_ERR_CUDA;
   *out = g_scratch_ptr[dev];
   return PA_OK;
 }
@@ -58,7 +64,7 @@ extern "C" pa_status pa_decode_static_scratch(
   if (!plan) return PA_ERR_INVALID_ARG;
   if (plan->scratch_bytes > pa::kStaticScratchBytes) return PA_ERR_SCRATCH_TOO_SMALL;
   void* scratch = nullptr;
-  const pa_status st = pa::static_scratch(&scratch);
+  const pa_status st = pa::static_scratch(static_cast<cudaStream_t>(stream), &scratch);
   if (st != PA_OK) return st;
   // The header (error word, split-arrival counters) must start at zero; the
   // split partials behind it are always written before they are read.

@@ -144,6 +144,21 @@ def test_decode_rejects_hand_edited_plans(lib):
     small = _plan(num_splits=1)
     small.scratch_bytes = 4096
     assert _decode_args(small, sbytes=4096) == pb.PA_ERR_SCRATCH_TOO_SMALL
+    # more splits (or a larger shape) than scratch_bytes was computed for: the
+    # partials would run past the buffer, so the plan is refused
+    more = _plan(num_splits=3)
+    more.max_splits = 5
+    more.grid[0] = 5
+    assert _decode_args(more) == pb.PA_ERR_INVALID_ARG
+    wider = _plan(num_splits=3)
+    wider.shape.max_batch = 128
+    assert _decode_args(wider) == pb.PA_ERR_INVALID_ARG
+    none = _plan(num_splits=3)
+    none.max_splits = 0
+    assert _decode_args(none) == pb.PA_ERR_INVALID_ARG
+    tile = _plan()
+    tile.tile_tokens *= 2
+    assert _decode_args(tile) == pb.PA_ERR_INVALID_ARG
 
 
 def test_decode_empty_batch_is_noop(lib):
@@ -227,3 +242,21 @@ def test_plan_decode_large_group_uses_head_groups(lib):
     assert q.grid[1] == 2 * 2
     e = _plan(mode=pb.MODE_EXTEND, num_q_heads=128, num_kv_heads=1, max_total_q=512)
     assert e.launches == 2
+
+
+def test_debug_wait_expiry_rejects_before_launch(lib):
+    vp = ctypes.c_void_p
+    L = pb.load()
+    assert L.pa_debug_wait_expiry(None, 0, 2_000_000, None) == pb.PA_ERR_INVALID_ARG
+    assert L.pa_debug_wait_expiry(vp(0x100000), 5, 2_000_000, None) == pb.PA_ERR_INVALID_ARG
+    assert L.pa_debug_wait_expiry(vp(0x100000), 0, 999, None) == pb.PA_ERR_INVALID_ARG
+    assert L.pa_debug_wait_expiry(vp(0x100000), 0, 10**8 + 1, None) == pb.PA_ERR_INVALID_ARG
+    assert L.pa_debug_wait_expiry(vp(0x100010), 0, 2_000_000, None) == pb.PA_ERR_UNSUPPORTED
+
+
+def test_device_code_bits_match_header(lib):
+    src = open(os.path.join(ROOT, "include", "pa.h")).read()
+    for name, val in (("WAIT_TIMEOUT", pb.DEVICE_WAIT_TIMEOUT), ("WORK_OVERFLOW", pb.DEVICE_WORK_OVERFLOW),
+                      ("CAPACITY", pb.DEVICE_CAPACITY), ("PAGE_ID", pb.DEVICE_PAGE_ID)):
+        m = re.search(r"PA_DEVICE_%s\s*=\s*(\d+)" % name, src)
+        assert m and int(m.group(1)) == val, name
