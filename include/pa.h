@@ -66,6 +66,20 @@ typedef enum {
   PA_ERR_DEVICE = 5             /* a kernel reported an error in the scratch header */
 } pa_status;
 
+/* Bits of the device error code that pa_check returns in *device_code.  A
+ * kernel ORs one into the scratch header when it meets the condition; it never
+ * traps.  Only an expired wait makes the other CTAs of the call give up; after
+ * any other bit the rest of the call still runs and writes its results. */
+typedef enum {
+  PA_DEVICE_WAIT_TIMEOUT = 1,   /* a bounded device-side wait ran out of time */
+  PA_DEVICE_WORK_OVERFLOW = 2,  /* a work list or block-table slice exceeded its planned capacity */
+  PA_DEVICE_CAPACITY = 4,       /* a length or query packing beyond what the plan allows; that
+                                   request's rows are left untouched */
+  PA_DEVICE_PAGE_ID = 8         /* a block-table entry of a page holding attended keys lies outside
+                                   [0, num_pages) (or an append slot's page does); that page reads
+                                   as zeros (is not written), every other page is unaffected */
+} pa_device_code;
+
 typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1 } pa_kv_dtype;
 /* VERIFY: extend where every request brings the same small number q_len of
  * new tokens (1 + speculative tokens) over a long context; planned and run
@@ -179,13 +193,22 @@ pa_status pa_decode(const pa_plan_t* plan,
  *   - The workspace is a 16 MiB array inside the library's device image,
  *     present on every GPU that loads the library until the process exits.
  *     Plans whose scratch_bytes exceed 16 MiB return PA_ERR_SCRATCH_TOO_SMALL.
- *   - The first call on each device looks up the array's device address (a
- *     runtime query, no allocation); make that first call before any stream
- *     capture.  Nothing is allocated, by this call or any later one.
+ *   - Every call made outside a stream capture looks up the array's device
+ *     address on the current device (a runtime query, no allocation); a call
+ *     made while its stream is being captured reuses the address the last
+ *     uncaptured call on that device found, so make the first call on each
+ *     device before any stream capture (without one, a captured call returns
+ *     PA_ERR_CUDA).  Nothing is allocated, by this call or any later one.
  *   - Every call on a device shares the one array and clears its error header
  *     first; calls that overlap on the GPU race on it, so the caller must
- *     serialise them.  Device-side error codes are not reported here; use
- *     pa_decode with pa_check when they are needed. */
+ *     serialise them.
+ *   - Device-side errors are not reported: the header that records them is
+ *     cleared by the next call and no call reads it.  In particular a request
+ *     whose seq_lens entry needs more KV splits than the plan allows (a length
+ *     beyond the capacity the plan was made for) is skipped on the device and
+ *     its rows of out and lse are LEFT UNTOUCHED, and the call still returns
+ *     PA_OK.  Callers that cannot rule this out on the host should use
+ *     pa_decode with pa_check, which reports it. */
 pa_status pa_decode_static_scratch(const pa_plan_t* plan,
                                    const void* q, int64_t q_stride_tok, int64_t q_stride_head,
                                    const void* k_cache, const void* v_cache,
@@ -261,9 +284,26 @@ pa_status pa_scratch_init(void* scratch, void* stream);
  * a device error).  Returns
  * PA_OK, PA_ERR_DEVICE (a kernel reported an error: a bounded wait expired,
  * a length or packing beyond what the plan allows, a work list over its
- * capacity, a slot outside the pool; the header's code bits are stored in
- * *device_code when non-NULL) or PA_ERR_CUDA. */
+ * capacity, a block-table entry or append slot outside the pool; the
+ * header's pa_device_code bits are stored in *device_code when non-NULL)
+ * or PA_ERR_CUDA. */
 pa_status pa_check(void* scratch, void* stream, uint32_t* device_code);
+
+/* Test hook for the device-side error reporting; callers of the attention
+ * calls never need it.  Enqueues one single-warp kernel that waits, through
+ * one of the bounded wait helpers the library's kernels use, on an mbarrier
+ * nothing arrives on, with no copy or tensor-core work in flight:
+ *   which 0: the decode kernels' suspending wait;
+ *         1: the extend kernel's suspending wait;  2: its polling wait;
+ *         3, 4: the same two after PA_DEVICE_WAIT_TIMEOUT is already set in
+ *               the header (as when another CTA's wait expired): they must
+ *               give up at once instead of waiting out their limit.
+ * The wait ends after limit_ns (1e3 .. 1e8 ns) of %globaltimer and sets
+ * PA_DEVICE_WAIT_TIMEOUT in the scratch header, which pa_check reports.  It
+ * also writes two int64 at byte 64 of the scratch: 1 if the wait saw the
+ * phase complete (never expected here) else 0, and the nanoseconds it waited.
+ * scratch: device, >= 65536 bytes, 256-byte aligned, header zeroed. */
+pa_status pa_debug_wait_expiry(void* scratch, int32_t which, int64_t limit_ns, void* stream);
 
 /* Static string for a status code. */
 const char* pa_status_string(pa_status status);

@@ -21,6 +21,12 @@ PA_ERR_SCRATCH_TOO_SMALL = 3
 PA_ERR_CUDA = 4
 PA_ERR_DEVICE = 5
 
+# bits of the device error code pa_check reports (pa_device_code)
+DEVICE_WAIT_TIMEOUT = 1
+DEVICE_WORK_OVERFLOW = 2
+DEVICE_CAPACITY = 4
+DEVICE_PAGE_ID = 8
+
 # bytes of the scratch header (error word, then split-arrival counters) at
 # the start of every scratch workspace
 SCRATCH_HEADER_BYTES = 65536
@@ -34,7 +40,8 @@ KV_BF16 = 0
 KV_FP8_E4M3 = 1
 
 EXPORTED_SYMBOLS = ("pa_plan", "pa_decode", "pa_extend", "pa_scratch_init", "pa_check",
-                    "pa_status_string", "pa_version", "pa_decode_static_scratch", "pa_append_kv")
+                    "pa_status_string", "pa_version", "pa_decode_static_scratch", "pa_append_kv",
+                    "pa_debug_wait_expiry")
 
 
 class PaShape(ctypes.Structure):
@@ -110,6 +117,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     L.pa_append_kv.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, i64, i32, i32, i32, i32, i32, vp, i32, f32, f32,
                                vp, vp]
     L.pa_append_kv.restype = ctypes.c_int
+    L.pa_debug_wait_expiry.argtypes = [vp, i32, i64, vp]
+    L.pa_debug_wait_expiry.restype = ctypes.c_int
     L.pa_scratch_init.argtypes = [vp, vp]
     L.pa_scratch_init.restype = ctypes.c_int
     L.pa_check.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -224,6 +233,12 @@ def append_kv(k_new, v_new, k_cache, v_cache, slot_mapping, *, kv_dtype: int = K
         k_cache.shape[0], k_cache.shape[1], k_cache.shape[2], k_cache.shape[3], int(kv_dtype), _ptr(slot_mapping),
         k_new.shape[0], float(k_scale), float(v_scale), _ptr(scratch), _stream(stream))
     _check(status, "pa_append_kv")
+
+
+def debug_wait_expiry(scratch, which: int, limit_ns: int, stream=None):
+    """pa_debug_wait_expiry: run one bounded device wait out on purpose (test hook)."""
+    _check(load().pa_debug_wait_expiry(_ptr(scratch), int(which), int(limit_ns), _stream(stream)),
+           "pa_debug_wait_expiry")
 
 
 def scratch_init(scratch, stream=None):

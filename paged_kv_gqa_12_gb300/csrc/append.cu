@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(256) append_kv_kernel(const AppendParams p) {
   const int64_t page = slot / p.page_size;
   const int64_t off = slot - page * p.page_size;
   if (page >= p.num_pages) {                              // outside the pool: nothing written
-    if (p.err != nullptr && vv == 0 && h == 0) atomicOr(p.err, kErrCapacity);
+    if (p.err != nullptr && vv == 0 && h == 0) atomicOr(p.err, kErrPageId);
     return;
   }
   const int64_t src = static_cast<int64_t>(t) * p.new_stride_tok + static_cast<int64_t>(h) * p.new_stride_head + vv * 8;

@@ -246,7 +246,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
   if (!bt_fits && tid == 0) atomicOr(p.err, kErrSchedOverflow);
   const int n_tiles = bt_fits ? tile_end - tile_begin : 0;
   const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
-  for (int i = tid; i < (bt_fits ? pg1 - pg0 : 0); i += kWarps * 32) bt_s[i] = bt_row[pg0 + i];
+  // A page id outside the pool becomes the out-of-range coordinate num_pages,
+  // whose TMA box reads as zeros; it is an error when the page holds attended
+  // keys (a page before the window start is fetched but wholly masked).
+  for (int i = tid; i < (bt_fits ? pg1 - pg0 : 0); i += kWarps * 32) {
+    int id = bt_row[pg0 + i];
+    if (static_cast<unsigned>(id) >= static_cast<unsigned>(p.num_pages)) {
+      if (((pg0 + i + 1) << ps_log2) > tok_lo) atomicOr(p.err, kErrPageId);
+      id = p.num_pages;
+    }
+    bt_s[i] = id;
+  }
   if (tid == 0) {
     prefetch_tensormap(&tmk);
     prefetch_tensormap(&tmv);

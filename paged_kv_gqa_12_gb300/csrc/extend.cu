@@ -217,41 +217,6 @@ __device__ __forceinline__ bool split_p_tile(int k0, int bn, int pos_min, int lo
   return !(k0 >= lo_max && k0 + bn - 1 <= pos_min && k0 + bn <= L);
 }
 
-// Bounded wait that also gives up as soon as any CTA has reported an error,
-// so one failure cannot make every later CTA wait out its own timeout.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if ((++spins & 255u) == 0 && *reinterpret_cast<volatile uint32_t*>(err) != 0u) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-      atomicOr(err, kErrWaitTimeout);
-      return false;
-    }
-  }
-  return true;
-}
-
-// The same bounded wait by polling, for the two MMA-issuing threads: they
-// react to a completed phase without a wake-up delay (measured +0.7 % over
-// the suspending wait), and only one thread of each polls.
-__device__ __forceinline__ bool poll_or_abort(uint64_t* bar, uint32_t parity, uint32_t* err) {
-  if (mbar_test_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (!mbar_test_wait(bar, parity)) {
-    if ((++spins & 255u) == 0) {
-      if (*reinterpret_cast<volatile uint32_t*>(err) != 0u) return false;
-      if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-        atomicOr(err, kErrWaitTimeout);
-        return false;
-      }
-    }
-  }
-  return true;
-}
-
 template <int D, int BN, int NST, int CPS, bool FP8 = false>
 struct ExtTraits {
   static constexpr int NCH = D / 64;                 // 128-byte column chunks per row
@@ -369,8 +334,12 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   }
   pdl_wait_primary();  // the scheduler's work list is complete and visible
   if (idx >= *p.work_count) return;
-  // another CTA already failed: leave (CTA-uniform, before any TMEM allocation)
-  if (__syncthreads_or(threadIdx.x == 0 && *reinterpret_cast<volatile uint32_t*>(p.err) != 0u)) return;
+  // another CTA's wait already expired: leave (CTA-uniform, before any TMEM
+  // allocation).  Other error bits (a bad request or page id) leave the rest
+  // of the call running.
+  if (__syncthreads_or(threadIdx.x == 0 &&
+                       (*reinterpret_cast<volatile uint32_t*>(p.err) & kErrWaitTimeout) != 0u))
+    return;
   const int2 item = p.work[idx];
   const int b = item.x;
   int qs, qlen, ctx, t0, t_end, lo_min, kt0, n;
@@ -449,10 +418,16 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     const int npg = BN >> ps_log2;
     // page coordinate of this lane's page of key tile j; pages with no
     // attended key are fetched out of bounds, where TMA writes zeros
+    // (and so are ids outside the pool, which are flagged: the rest of the
+    // call is unaffected)
     auto page_coord = [&](int j) {
       const int pg = (((kt0 + j) * BN) >> ps_log2) + lane;
       const bool outside = (pg * ps >= L) || ((pg + 1) * ps <= lo_min);
-      return outside ? p.num_pages : bt_row[pg];
+      if (outside) return p.num_pages;
+      const int id = bt_row[pg];
+      if (static_cast<unsigned>(id) < static_cast<unsigned>(p.num_pages)) return id;
+      atomicOr(p.err, kErrPageId);
+      return p.num_pages;
     };
     if constexpr (!FP8) {
       for (int j = 0; j < n && ok; ++j) {
@@ -847,6 +822,7 @@ struct KvCopyParams {
   uint16_t* kc;
   uint16_t* vc;
   int32_t* bt_copy;
+  uint32_t* err;   // scratch header error word
 };
 
 template <int D>
@@ -872,7 +848,9 @@ __global__ void __launch_bounds__(256) extend_kv_copy_kernel(const KvCopyParams 
   uint4* kd = reinterpret_cast<uint4*>(p.kc + dst_page * page_elems);
   uint4* vd = reinterpret_cast<uint4*>(p.vc + dst_page * page_elems);
   if (src < 0 || src >= p.num_pages) {
-    // a page id outside the pool reads as zeros, as a TMA box outside it does
+    // a page id outside the pool reads as zeros, as a TMA box outside it
+    // does, and is flagged
+    if (threadIdx.x == 0) atomicOr(p.err, kErrPageId);
     for (int u = threadIdx.x; u < 2 * units; u += blockDim.x) {
       kd[u] = make_uint4(0, 0, 0, 0);
       vd[u] = make_uint4(0, 0, 0, 0);
@@ -1062,6 +1040,7 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
     cp.kc = reinterpret_cast<uint16_t*>(kc);
     cp.vc = reinterpret_cast<uint16_t*>(vc);
     cp.bt_copy = bt_copy;
+    cp.err = reinterpret_cast<uint32_t*>(sc);
     const dim3 cgrid(static_cast<unsigned>(maxp), static_cast<unsigned>(batch));
     switch (s.head_dim) {
       case 64: extend_kv_copy_kernel<64><<<cgrid, 256, 0, strm>>>(cp); break;

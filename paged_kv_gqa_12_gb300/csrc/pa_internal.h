@@ -16,10 +16,11 @@ namespace pa {
 constexpr int64_t kScratchHeaderBytes = 65536;
 constexpr int64_t kMergeCounterOffset = 256;
 constexpr int64_t kMergeCounters = (kScratchHeaderBytes - kMergeCounterOffset) / 4;
-// Device error codes OR-ed into the header's first word.
-constexpr uint32_t kErrWaitTimeout = 1u;        // an mbarrier wait ran out of time
-constexpr uint32_t kErrSchedOverflow = 2u;      // extend work list exceeded its capacity
-constexpr uint32_t kErrCapacity = 4u;           // a length exceeded the plan's capacity
+// Device error codes OR-ed into the header's first word (pa_device_code).
+constexpr uint32_t kErrWaitTimeout = PA_DEVICE_WAIT_TIMEOUT;     // an mbarrier wait ran out of time
+constexpr uint32_t kErrSchedOverflow = PA_DEVICE_WORK_OVERFLOW;  // a work list exceeded its capacity
+constexpr uint32_t kErrCapacity = PA_DEVICE_CAPACITY;            // a length exceeded the plan's capacity
+constexpr uint32_t kErrPageId = PA_DEVICE_PAGE_ID;               // a page id outside the pool
 // Wall-clock bound on every device-side wait (nanoseconds of %globaltimer).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
 
@@ -31,6 +32,7 @@ struct DecodeParams {
   int64_t bt_stride;
   const int32_t* seq_lens;
   int batch, num_q_heads, num_kv_heads, group, page_size;
+  int num_pages;              // pool size: block-table entries must lie in [0, num_pages)
   float scale_log2;           // scale * log2(e)
   float cap_log2;             // soft_cap * log2(e); 0 = off
   float scale_over_cap;       // scale / soft_cap

@@ -73,7 +73,7 @@ def test_append_reports_slot_outside_pool(pb):
     plan = gh.make_plan(base)
     scratch = pb.alloc_scratch(plan)
     pb.append_kv(kt, vt, d["k"], d["v"], torch.from_numpy(slots).cuda(), scratch=scratch)
-    assert pb.check(scratch) != 0
+    assert pb.check(scratch) == pb.DEVICE_PAGE_ID
     k = d["k"].cpu().view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(k[0, 0], k_new[0]) and np.array_equal(k[1, 1], k_new[2])
 
