@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(OUT_DIR, "libpa_gb300.so")
-SOURCES = ["api.cu", "decode.cu", "extend.cu", "decode_static.cu", "append.cu"]
+SOURCES = ["api.cu", "decode.cu", "extend.cu", "decode_static.cu", "append.cu", "debug.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC,
               "--expt-relaxed-constexpr"] + ARCH

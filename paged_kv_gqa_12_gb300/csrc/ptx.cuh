@@ -69,14 +69,52 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete, for at most
-// kWaitTimeoutNs; on expiry OR `code` into *err and return false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
+// limit_ns; on expiry OR kErrWaitTimeout into *err and return false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(err, kErrWaitTimeout);
       return false;
+    }
+  }
+  return true;
+}
+
+// Bounded wait that also gives up as soon as any CTA has reported an expired
+// wait, so one failure cannot make every later CTA wait out its own timeout.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                              uint64_t limit_ns = kWaitTimeoutNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 255u) == 0 && (*reinterpret_cast<volatile uint32_t*>(err) & kErrWaitTimeout) != 0u) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicOr(err, kErrWaitTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+// The same bounded wait by polling, for threads that must react to a
+// completed phase without a wake-up delay (the tensor-core issuers): only one
+// thread of a warp should poll.
+__device__ __forceinline__ bool poll_or_abort(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                              uint64_t limit_ns = kWaitTimeoutNs) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (!mbar_test_wait(bar, parity)) {
+    if ((++spins & 255u) == 0) {
+      if ((*reinterpret_cast<volatile uint32_t*>(err) & kErrWaitTimeout) != 0u) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        atomicOr(err, kErrWaitTimeout);
+        return false;
+      }
     }
   }
   return true;

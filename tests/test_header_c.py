@@ -37,6 +37,7 @@ int main(void) {
                  p, 0, 0, lse, p, plan.scratch_bytes, p);
   st = pa_append_kv(p, p, 0, 0, p, p, 0, 0, 0, 0, 16, 8, 128, PA_KV_BF16, (const int64_t*)0, 0,
                     1.f, 1.f, p, p);
+  st = pa_debug_wait_expiry(p, 0, 0, p);   /* null scratch: refused on the host */
   (void)pa_scratch_init;
   (void)pa_check;
   (void)code;
