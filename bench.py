@@ -138,31 +138,106 @@ def weak_scaling_throughput(world: int, steps: int, units_per_step: float, secon
 
 # ---- clocks -----------------------------------------------------------------------
 
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+_NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
 class ClockSampler:
-    """nvidia-smi sampled every 50 ms on a background thread; samples are
-    timestamped on arrival so the timed window can be cut out afterwards."""
+    """SM clock, power and clock-event reasons sampled every millisecond on a
+    background thread through NVML (read-only queries), timestamped on
+    arrival, so the timed window -- even a 10 ms one -- can be cut out
+    afterwards.  Falls back to ``nvidia-smi -lms 50`` where NVML cannot be
+    loaded.  The GPU is found by its PCI bus id, so CUDA_VISIBLE_DEVICES
+    renumbering does not matter."""
 
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.samples = []
+    def __init__(self, cuda_index: int, period_s: float = 0.001):
+        self.samples = []      # (time, sm_mhz, power_w, [reasons])
+        self.max_mhz = None
+        self.source = None
         self.proc = None
+        self._stop = threading.Event()
+        self.period = period_s
+        if self._nvml_open(cuda_index):
+            self.source = "nvml, 1 ms"
+            self.t = threading.Thread(target=self._nvml_loop, daemon=True)
+            self.t.start()
+            return
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                ["nvidia-smi", "-i", str(cuda_index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
                  "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             return
-        self.t = threading.Thread(target=self._read, daemon=True)
+        self.source = "nvidia-smi, 50 ms"
+        self.t = threading.Thread(target=self._smi_loop, daemon=True)
         self.t.start()
 
-    def _read(self):
+    def _nvml_open(self, cuda_index):
+        import ctypes
+        try:
+            import torch
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return False
+            h = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(cuda_index)
+            bus = getattr(props, "pci_bus_id", None)
+            ok = False
+            if bus is not None:
+                pci = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), bus,
+                                             getattr(props, "pci_device_id", 0))
+                ok = nv.nvmlDeviceGetHandleByPciBusId_v2(pci.encode(), ctypes.byref(h)) == 0
+            if not ok:
+                ok = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(cuda_index), ctypes.byref(h)) == 0
+            if not ok:
+                return False
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # NVML_CLOCK_SM
+                self.max_mhz = float(mx.value)
+            self._nv, self._h = nv, h
+            return True
+        except (OSError, AttributeError, RuntimeError):
+            return False
+
+    def _nvml_loop(self):
+        import ctypes
+        nv, h = self._nv, self._h
+        clk, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            t = time.time()
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                p = pw.value / 1000.0 if nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 else None
+                rv = rs.value if reasons_fn(h, ctypes.byref(rs)) == 0 else 0
+                r = [n for bit, n in _NVML_REASONS.items() if rv & bit]
+                self.samples.append((t, float(clk.value), p, r))
+            self._stop.wait(self.period)
+
+    def _smi_loop(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.proc.stdout:
-            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+            r = [x.strip() for x in line.split(",")]
+            if len(r) < 8:
+                continue
+            try:
+                sm, mx = float(r[0]), float(r[1])
+            except ValueError:
+                continue
+            try:
+                p = float(r[2])
+            except ValueError:
+                p = None
+            self.max_mhz = mx
+            self.samples.append((time.time(), sm, p, [names[i] for i in range(4) if r[4 + i].lower().startswith("active")]))
 
     def stop(self):
+        self._stop.set()
         if self.proc:
             self.proc.terminate()
             try:
@@ -171,22 +246,22 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0, t1):
-        rows = [s for (t, s) in self.samples if t0 <= t <= t1 and len(s) >= 8]
+        """Clock record of the timed window [t0, t1].  If no sample fell inside
+        it, the record says so and summarises the whole run instead."""
+        rows = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed region"
         if not rows:
-            rows = [s for (_, s) in self.samples if len(s) >= 8]
+            rows = list(self.samples)
+            window = "whole run: no sample fell inside the timed region"
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower().startswith("active")})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][1]),
-                "power_w_max": max((num(r[2]) or 0.0) for r in rows), "reasons": reasons, "samples": len(rows)}
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["no clock samples"], "samples": 0,
+                    "source": self.source}
+        sm = [r[1] for r in rows]
+        pw = [r[2] for r in rows if r[2] is not None]
+        reasons = sorted({n for r in rows for n in r[3]})
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(rows),
+                "window": window, "window_ms": round((t1 - t0) * 1e3, 3), "source": self.source}
 
 
 # ---- our arm ------------------------------------------------------------------------
@@ -230,11 +305,12 @@ def run_ours(args):
     dout = torch.empty(dp.q.shape, dtype=torch.bfloat16, device=dev)
     dlse = torch.empty(dp.q.shape[:2], dtype=torch.float32, device=dev)
     extend_ok = args.only != "decode"
+    eplan_kw = dict(mode=pb.MODE_EXTEND, num_q_heads=ep.num_q_heads, num_kv_heads=ep.num_kv_heads,
+                    head_dim=ep.head_dim, page_size=ep.page_size, kv_dtype=pb.KV_BF16, max_batch=ep.batch,
+                    max_pages_per_seq=ep.block_table.shape[1], max_total_q=ep.num_rows,
+                    window=ep.window, has_sinks=ep.sinks is not None, soft_cap=ep.soft_cap)
     try:
-        eplan = pb.plan(mode=pb.MODE_EXTEND, num_q_heads=ep.num_q_heads, num_kv_heads=ep.num_kv_heads,
-                        head_dim=ep.head_dim, page_size=ep.page_size, kv_dtype=pb.KV_BF16, max_batch=ep.batch,
-                        max_pages_per_seq=ep.block_table.shape[1], max_total_q=ep.num_rows,
-                        window=ep.window, has_sinks=ep.sinks is not None, soft_cap=ep.soft_cap)
+        eplan = pb.plan(**eplan_kw)
         escr = pb.alloc_scratch(eplan, dev)
     except pb.PaError:
         extend_ok = False
@@ -332,6 +408,50 @@ def run_ours(args):
     h2d = hq.numel() * 2 + hbt.numel() * 4 + hsl.numel() * 4
     d2h = hout.numel() * 2 + hlse.numel() * 4
 
+    # extend end to end: pinned-host q and metadata in, pa_plan + pa_extend,
+    # out and lse back, every step
+    e2e_ext = None
+    if extend_ok:
+        xq = torch.from_numpy(ep.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+        xbt = torch.from_numpy(ep.block_table).pin_memory()
+        xsl = torch.from_numpy(ep.seq_lens).pin_memory()
+        xqsl = torch.from_numpy(ep.query_start_loc).pin_memory()
+        xout = torch.empty(ep.q.shape, dtype=torch.bfloat16).pin_memory()
+        xlse = torch.empty(ep.q.shape[:2], dtype=torch.float32).pin_memory()
+        gxq, gxbt = torch.empty_like(ed["q"]), torch.empty_like(ed["bt"])
+        gxsl, gxqsl = torch.empty_like(ed["sl"]), torch.empty_like(ed["qsl"])
+
+        def e2e_ext_step():
+            gxq.copy_(xq, non_blocking=True)
+            gxbt.copy_(xbt, non_blocking=True)
+            gxsl.copy_(xsl, non_blocking=True)
+            gxqsl.copy_(xqsl, non_blocking=True)
+            plan = pb.plan(**eplan_kw)
+            pb.extend(plan, gxq, ed["k"], ed["v"], gxbt, gxsl, gxqsl, scale=ep.scale, out=eout, lse=else_,
+                      sinks=ed["sinks"], k_scale=ep.k_scale, v_scale=ep.v_scale, scratch=escr, stream=stream)
+            xout.copy_(eout, non_blocking=True)
+            xlse.copy_(else_, non_blocking=True)
+
+        Kx = min(K, 50)
+        for _ in range(3):
+            e2e_ext_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        e0.record(stream)
+        for _ in range(Kx):
+            e2e_ext_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        xs = max_over_ranks([e0.elapsed_time(e1) / 1e3], dist if world > 1 else None, dev)[0]
+        e2e_ext = {"value": round(weak_scaling_throughput(world, Kx, extend_flops(ep), xs) / 1e12, 2),
+                   "unit": "TFLOP/s", "steps": Kx,
+                   "h2d_bytes_per_step": int(xq.numel() * 2 + xbt.numel() * 4 + xsl.numel() * 4 + xqsl.numel() * 4),
+                   "d2h_bytes_per_step": int(xout.numel() * 2 + xlse.numel() * 4),
+                   "what": "extend through the C ABI: pinned-host q/block_table/seq_lens/query_start_loc H2D, "
+                           "pa_plan, pa_extend, out/lse D2H"}
+        if pb.check(escr) != 0:
+            raise RuntimeError("device error during the extend end-to-end loop")
+
     # the extras are stated for the default decode workload's sequences
     extras = None if args.no_extras or args.decode_workload != DECODE_WORKLOAD or args.decode_splits else \
         measure_extras(pb, wl, dp, dd, dev, stream)
@@ -371,7 +491,8 @@ def run_ours(args):
     roof = {k: v for k, v in kernels[dominant].items() if k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
     roof["kernel"] = dominant
 
-    cpu = cpu_baseline(dp, args.cpu_sample) if (world == 1 and not args.no_cpu_baseline) else None
+    cpu = cpu_baseline(dp, ep if extend_ok else None, args.cpu_sample) \
+        if (world == 1 and not args.no_cpu_baseline) else None
     clocks = sampler.summary(t0, t1) if sampler else None
     line = {
         "metric": "paged decode KV-read TB/s (% of HBM peak); extend TFLOP/s (% bf16 peak)",
@@ -399,7 +520,8 @@ def run_ours(args):
         "kernels": kernels,
         "e2e": {"value": round(weak_scaling_throughput(world, Ke, dbytes, e2e_s) / 1e12, 4), "unit": "TB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "what": "decode through the C ABI: pinned-host q/block_table/seq_lens H2D, pa_plan, pa_decode, out/lse D2H"}
+                "what": "decode through the C ABI: pinned-host q/block_table/seq_lens H2D, pa_plan, pa_decode, out/lse D2H",
+                "extend": e2e_ext}
                if e2e_s is not None else None,
         "gpu_launches": K * ((dplan.launches if decode_on else 0) + (eplan.launches if extend_ok else 0)),
         "extras": extras,
@@ -519,11 +641,16 @@ def measure_extras(pb, wl, dp, dd, dev, stream):
 
 # ---- CPU oracle legs --------------------------------------------------------------
 
-def cpu_baseline(p, n_requests: int, min_seconds: float = 10.0):
-    """The oracle, as it stands, on a bounded sample of the decode workload:
-    the first n_requests requests (all heads), on all host cores, repeated
-    until about min_seconds of CPU work have been timed (at least 3 passes)."""
+def cpu_baseline(p, ep, n_requests: int, min_seconds: float = 6.0):
+    """The oracle, as it stands, on bounded samples of the step's workloads,
+    on the host cores: the decode batch (its first n_requests requests, all
+    heads; all cores, repeated until about min_seconds have been timed, at
+    least 3 passes), whole requests of the extend workload (all cores; the
+    shortest requests in batch order until about a fifth of the workload's
+    FLOPs), and the tiny decode workload on one core.  ``value`` is the
+    decode figure, in the unit of the benchmark's metric."""
     import oracle
+    from paged_kv_gqa_12_gb300 import workloads as wl
     rows = np.arange(min(n_requests, p.batch), dtype=np.int32)
     cores = os.cpu_count() or 1
     oracle.attention(p, rows=rows[:1], num_threads=cores)  # load + warm
@@ -534,10 +661,46 @@ def cpu_baseline(p, n_requests: int, min_seconds: float = 10.0):
         dt += time.perf_counter() - t
         passes += 1
     sub = sample_bytes(p, rows) * passes
-    return {"value": round(sub / dt / 1e12, 9), "unit": "TB/s", "cores": cores, "kind": "oracle",
-            "seconds": round(dt, 3),
-            "sample": f"decode requests 0..{len(rows) - 1} of the same workload (all {p.num_q_heads} heads), "
-                      f"{sub // passes} algorithmic bytes per pass, {passes} passes"}
+    res = {"value": round(sub / dt / 1e12, 9), "unit": "TB/s", "cores": cores, "kind": "oracle",
+           "seconds": round(dt, 3),
+           "sample": f"decode requests 0..{len(rows) - 1} of the same workload (all {p.num_q_heads} heads), "
+                     f"{sub // passes} algorithmic bytes per pass, {passes} passes"}
+    if ep is not None:
+        # extend: whole requests, smallest first, until a fifth of the FLOPs
+        import dataclasses
+        qsl = ep.query_start_loc
+        per_req = [extend_flops(dataclasses.replace(ep, seq_lens=ep.seq_lens[b:b + 1],
+                                                    query_start_loc=np.array([0, qsl[b + 1] - qsl[b]], np.int32)))
+                   for b in range(ep.batch)]
+        total = sum(per_req)
+        chosen, fl = [], 0
+        for b in sorted(range(ep.batch), key=lambda b: per_req[b]):
+            if fl >= total / 5:
+                break
+            chosen.append(b)
+            fl += per_req[b]
+        chosen.sort()
+        erows = np.concatenate([np.arange(qsl[b], qsl[b + 1]) for b in chosen]).astype(np.int32)
+        t = time.perf_counter()
+        oracle.attention(ep, rows=erows, num_threads=cores)
+        et = time.perf_counter() - t
+        res["extend"] = {"value": round(fl / et / 1e12, 9), "unit": "TFLOP/s", "gflops": round(fl / et / 1e9, 3),
+                         "cores": cores, "kind": "oracle", "seconds": round(et, 3),
+                         "sample": f"extend requests {chosen} of the extend workload (whole requests, all "
+                                   f"{ep.num_q_heads} heads), {fl} algorithmic FLOPs ({fl / total:.1%} of the call)"}
+    tp = wl.workload_problem("decode_tiny")
+    passes, dt = 0, 0.0
+    while passes < 3 or dt < 2.0:
+        t = time.perf_counter()
+        oracle.attention(tp, num_threads=1)
+        dt += time.perf_counter() - t
+        passes += 1
+    tb = decode_bytes(tp)
+    res["decode_tiny_one_core"] = {"value": round(tb * passes / dt / 1e12, 9), "unit": "TB/s", "cores": 1,
+                                   "kind": "oracle", "ms_per_call": round(dt / passes * 1e3, 4),
+                                   "sample": f"the whole tiny decode workload ({tb} algorithmic bytes), "
+                                             f"{passes} passes"}
+    return res
 
 
 def sample_bytes(p, rows):

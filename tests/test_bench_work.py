@@ -47,3 +47,17 @@ def test_decode_plan_arguments_follow_the_workload():
     e4 = wl.workload_problem("decode_e4m3_window", batch=2)
     kw = bench.decode_plan_kw(pb, e4, "decode_e4m3_window")
     assert kw["kv_dtype"] == pb.KV_FP8_E4M3 and kw["window"] == 1024 and kw["has_sinks"] and kw["num_splits"] == 0
+
+
+def test_clock_summary_marks_its_window():
+    # samples inside the timed window are summarised as such; with none
+    # inside, the record says it falls back to the whole run
+    import bench
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.max_mhz, s.source = 2070.0, "test"
+    s.samples = [(1.0, 2070.0, 500.0, []), (2.0, 1900.0, 900.0, ["sw_power_cap"]), (3.0, 2070.0, 600.0, [])]
+    inside = s.summary(1.5, 2.5)
+    assert inside["window"] == "timed region" and inside["samples"] == 1
+    assert inside["sm_mhz"] == 1900.0 and inside["reasons"] == ["sw_power_cap"]
+    outside = s.summary(10.0, 10.01)
+    assert outside["window"].startswith("whole run") and outside["samples"] == 3
