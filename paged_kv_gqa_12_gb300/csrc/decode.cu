@@ -44,6 +44,9 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr float kLog2e = 1.4426950408889634f;
+// A tile is computed with exact weights (P = P_hi + P_lo) when some row's
+// largest weight from it exceeds 1 / kHotShare of the row's denominator.
+constexpr float kHotShare = 8.f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Attended keys of request b and their split partition.  Splits are
@@ -169,7 +172,7 @@ __device__ __forceinline__ void merge_splits(const DecodeParams& p, int n_splits
   }
 }
 
-template <int D, bool FP8, int NH8, int TS, int NS>
+template <int D, bool FP8, int NH8, int TS, int NS, bool CAP>
 __global__ void __launch_bounds__(kWarps * 32)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                     const DecodeParams p) {
@@ -328,6 +331,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
       for (int e = 0; e < 4; ++e) o[i][j][e] = 0.f;
   float m_run[NH8][2], l_run[NH8][2];
   int rpos[NH8][2], rlo[NH8][2];   // this thread's two rows: last and first attended key
+  bool rvalid[NH8][2];             // the row is a real (token, head), not MMA padding
 #pragma unroll
   for (int j = 0; j < NH8; ++j) {
     m_run[j][0] = m_run[j][1] = -INFINITY;
@@ -335,6 +339,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int rr = j * 8 + 2 * c + h;
+      rvalid[j][h] = rr < R;
       rpos[j][h] = pos_first + min(rr, R - 1) / Gc;
       rlo[j][h] = p.window > 0 ? rpos[j][h] - p.window + 1 : 0;
     }
@@ -348,10 +353,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
   }
   __syncwarp();
 
-  const bool capped = p.cap_log2 > 0.f;
   // e4m3 descales of this request (per request when given, else per tensor)
-  const float k_sc = p.k_scales != nullptr ? p.k_scales[b] : p.k_scale;
-  const float v_sc = p.v_scales != nullptr ? p.v_scales[b] : p.v_scale;
+  const uint64_t k_sc2 = dequant_scale2(p.k_scales != nullptr ? p.k_scales[b] : p.k_scale);
+  const uint64_t v_sc2 = dequant_scale2(p.v_scales != nullptr ? p.v_scales[b] : p.v_scale);
+  bool l_small = true;   // some row's running denominator (summed over its lanes) is below kHotShare
   int it = 0;
   for (int k = warp; k < n_tiles; k += kWarps, ++it) {
     const int stage = it % NS;
@@ -396,10 +401,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
 #pragma unroll
         for (int ks = 0; ks < T::KS; ++ks) {
           uint32_t a[4];
-          a[0] = dequant_e4m3x2(w0[ks], k_sc);
-          a[1] = dequant_e4m3x2(w1[ks], k_sc);
-          a[2] = dequant_e4m3x2(w0[ks] >> 16, k_sc);
-          a[3] = dequant_e4m3x2(w1[ks] >> 16, k_sc);
+          a[0] = dequant_e4m3x2<0>(w0[ks], k_sc2);
+          a[1] = dequant_e4m3x2<0>(w1[ks], k_sc2);
+          a[2] = dequant_e4m3x2<1>(w0[ks], k_sc2);
+          a[3] = dequant_e4m3x2<1>(w1[ks], k_sc2);
 #pragma unroll
           for (int j = 0; j < NH8; ++j) mma_bf16(s[mt][j], a, qf[ks][j][0], qf[ks][j][1]);
         }
@@ -410,21 +415,35 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
     float mx[NH8][2];
 #pragma unroll
     for (int j = 0; j < NH8; ++j) mx[j][0] = mx[j][1] = -INFINITY;
+    // the soft-cap is compiled in only where a call uses it, and the mask
+    // only into the version that masked tiles take
+    auto scores = [&](auto masked_tag) {
+      constexpr bool MASKED = decltype(masked_tag)::value;
 #pragma unroll
-    for (int mt = 0; mt < T::MT; ++mt)
+      for (int mt = 0; mt < T::MT; ++mt)
 #pragma unroll
-      for (int j = 0; j < NH8; ++j)
+        for (int j = 0; j < NH8; ++j)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float v = s[mt][j][e];
-          v = capped ? p.cap_log2 * tanhf(v * p.scale_over_cap) : v * p.scale_log2;
-          if (partial) {
-            const int tok = t0 + mt * 16 + g + ((e >> 1) << 3);
-            if (tok < tok_lo || tok >= tok_hi || tok > rpos[j][e & 1] || tok < rlo[j][e & 1]) v = -INFINITY;
+          for (int e = 0; e < 4; ++e) {
+            float v = s[mt][j][e];
+            if constexpr (CAP) {
+              v = p.cap_log2 * tanhf(v * p.scale_over_cap);
+            } else {
+              v *= p.scale_log2;
+            }
+            if constexpr (MASKED) {
+              const int tok = t0 + mt * 16 + g + ((e >> 1) << 3);
+              if (tok < tok_lo || tok >= tok_hi || tok > rpos[j][e & 1] || tok < rlo[j][e & 1]) v = -INFINITY;
+            }
+            s[mt][j][e] = v;
+            mx[j][e & 1] = fmaxf(mx[j][e & 1], v);
           }
-          s[mt][j][e] = v;
-          mx[j][e & 1] = fmaxf(mx[j][e & 1], v);
-        }
+    };
+    if (partial) {
+      scores(std::true_type{});
+    } else {
+      scores(std::false_type{});
+    }
     float alpha[NH8][2], mu[NH8][2];
     bool grew = false;   // some row's running maximum rose (else every alpha is ex2(0) = 1)
 #pragma unroll
@@ -435,6 +454,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        mx[j][h] = m;   // the row's largest score in this tile
         const float m_new = fmaxf(m_run[j][h], m);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         grew |= m_new > m_run[j][h];
@@ -469,17 +489,42 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         }
       }
     }
+    // Does some row take more than 1/kHotShare of its (warp's) running
+    // denominator from one key of this tile?  The denominator only grows, so
+    // such a share bounds the key's final weight.  Weights here are at most 1
+    // (every row's maximum is exact), so a tile where no row's maximum rose
+    // cannot be hot once every row's denominator is at least kHotShare: the
+    // lane reduction of the denominators runs only on the other tiles.
+    bool hot = false;
+    if (rescale || l_small) {
+      bool small = false;
+#pragma unroll
+      for (int j = 0; j < NH8; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float l = l_run[j][h];
+          l += __shfl_xor_sync(0xffffffffu, l, 4);
+          l += __shfl_xor_sync(0xffffffffu, l, 8);
+          l += __shfl_xor_sync(0xffffffffu, l, 16);
+          hot |= rvalid[j][h] && ex2(mx[j][h] - mu[j][h]) * kHotShare > l;
+          small |= rvalid[j][h] && l < kHotShare;
+        }
+      hot = __any_sync(0xffffffffu, hot);
+      l_small = __any_sync(0xffffffffu, small);
+    }
 
     // ---- O^T += V^T P^T -----------------------------------------------------
-    // On tiles where some row masks a key (sequence start or end, window edge,
-    // a verify row's own position) P = P_hi + P_lo, both bf16: two MMAs make
-    // the weights exact to ~2^-17 (one bf16 P can be 2^-9 off, which a row
-    // with few attended keys does not average out), and masked keys' V rows
-    // are zeroed.  Every row of an unmasked tile attends to all its keys and
-    // to the tiles before it: one bf16 P, no masks.  Two compiled versions,
-    // chosen per tile.
-    auto pv = [&](auto exact_tag) {
+    // P = P_hi + P_lo, both bf16 (two MMAs, weights exact to ~2^-17), on
+    // tiles where some row masks a key (sequence start or end, window edge, a
+    // verify row's own position; masked keys' V rows are zeroed there) or
+    // where some row's largest weight from this tile exceeds 1/kHotShare of
+    // its running denominator.  One bf16 P is up to 2^-8 off per weight, which
+    // a row does not average out when a few keys carry its weight; on the
+    // other tiles every key's final weight is below 1/kHotShare and one bf16
+    // P, with no masks, is used.  Three compiled versions, chosen per tile.
+    auto pv = [&](auto exact_tag, auto mask_tag) {
       constexpr bool EXACT = decltype(exact_tag)::value;
+      constexpr bool MASK = decltype(mask_tag)::value;   // (masked tiles are always exact)
 #pragma unroll
       for (int mt = 0; mt < T::MT; ++mt) {
         uint32_t pb[NH8][2], pl[NH8][2];
@@ -501,7 +546,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
         // Masked keys have P = 0, but their V rows may be stale or NaN: zero
         // them in the fragment so 0 * NaN never reaches the accumulator.
         uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-        if constexpr (EXACT) {
+        if constexpr (MASK) {
           const int tk = t0 + mt * 16 + 2 * c;
           auto valid = [&](int t) { return t >= tok_lo && t < tok_hi; };
           vm_lo = (valid(tk) ? 0x0000ffffu : 0u) | (valid(tk + 1) ? 0xffff0000u : 0u);
@@ -514,7 +559,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
           for (int i = 0; i < T::KS; ++i) {
             uint32_t a[4];
             ldsm_x4_t(a, vst_u + T::off(tok, (i * 16 + ((mi & 1) << 3)) * 2));
-            if constexpr (EXACT) {
+            if constexpr (MASK) {
               a[0] &= vm_lo;
               a[1] &= vm_lo;
               a[2] &= vm_hi;
@@ -550,11 +595,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
             const uint32_t x = __byte_perm(ra[i >> 1], rb[i >> 1], sel);
             const uint32_t y = __byte_perm(rc[i >> 1], rd[i >> 1], sel);
             uint32_t a[4];
-            a[0] = dequant_e4m3x2(x, v_sc);
-            a[1] = dequant_e4m3x2(x >> 16, v_sc);
-            a[2] = dequant_e4m3x2(y, v_sc);
-            a[3] = dequant_e4m3x2(y >> 16, v_sc);
-            if constexpr (EXACT) {
+            a[0] = dequant_e4m3x2<0>(x, v_sc2);
+            a[1] = dequant_e4m3x2<1>(x, v_sc2);
+            a[2] = dequant_e4m3x2<0>(y, v_sc2);
+            a[3] = dequant_e4m3x2<1>(y, v_sc2);
+            if constexpr (MASK) {
               a[0] &= vm_lo;
               a[1] &= vm_lo;
               a[2] &= vm_hi;
@@ -570,9 +615,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_consta
       }
     };
     if (partial) {
-      pv(std::true_type{});
+      pv(std::true_type{}, std::true_type{});
+    } else if (hot) {
+      pv(std::true_type{}, std::false_type{});
     } else {
-      pv(std::false_type{});
+      pv(std::false_type{}, std::false_type{});
     }
 
     __syncwarp();
@@ -738,7 +785,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeParams p)
 template <int D, bool FP8, int NH8, int TS, int NS>
 cudaError_t launch_variant(const CUtensorMap& tmk, const CUtensorMap& tmv, const DecodeParams& p, dim3 grid,
                            int smem, cudaStream_t stream) {
-  auto kern = decode_split_kernel<D, FP8, NH8, TS, NS>;
+  auto kern = p.cap_log2 > 0.f ? decode_split_kernel<D, FP8, NH8, TS, NS, true>
+                               : decode_split_kernel<D, FP8, NH8, TS, NS, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (grid.x > 0 && grid.y > 0 && grid.z > 0) {

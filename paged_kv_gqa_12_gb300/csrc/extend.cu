@@ -49,6 +49,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "extend.h"
 #include "pa_internal.h"
@@ -203,19 +204,15 @@ __device__ __forceinline__ float tanh_exp2(float x) {
   return 1.f - __fdividef(2.f, e + 1.f);
 }
 
-// A key tile in which some query row of the item masks some key (causal
-// diagonal, window edge or sequence end), in an item where some row attends
-// fewer than kExactKeys keys in all.  There the softmax weights are passed as
-// P = P_hi + P_lo (two bf16 halves, two PV MMAs): one bf16 P (2^-9 relative)
-// is not averaged out over a few keys.  Rows of an item whose first row
-// already attends kExactKeys keys (min(position + 1, window) of them) take
-// one bf16 P on every tile, as they do on their unmasked tiles.
-constexpr int kExactKeys = 128;
-__device__ __forceinline__ bool split_p_tile(int k0, int bn, int pos_min, int lo_max, int L, int window) {
-  const int min_keys = window > 0 ? min(pos_min + 1, window) : pos_min + 1;
-  if (min_keys >= kExactKeys) return false;
-  return !(k0 >= lo_max && k0 + bn - 1 <= pos_min && k0 + bn <= L);
-}
+// Exact softmax weights on a key tile: P = P_hi + P_lo (two bf16 halves, two
+// PV MMAs, exact to ~2^-17) when some query row's largest weight from the
+// tile exceeds 1 / kHotShare of its running denominator (a row that attends
+// few keys, or whose weight sits on a few dominant keys).  One bf16 P is up to
+// 2^-8 off per weight, which such rows do not average out; the denominator
+// only grows, so every key of a tile given one bf16 P ends with a final
+// weight below 1 / kHotShare.  Each softmax warp flags the tiles where one
+// of its rows needs it; the PV issuer adds the P_lo pass when any did.
+constexpr float kHotShare = 8.f;
 
 template <int D, int BN, int NST, int CPS, bool FP8 = false>
 struct ExtTraits {
@@ -257,8 +254,10 @@ struct ExtTraits {
     return (static_cast<unsigned>(j) / static_cast<unsigned>(NSB)) & 1u;
   }
   // mbarriers: q_full, six per ring stage, s_full/p_full/o_done per S
-  // buffer, q_moved (Q in TMEM); then the TMEM address
-  static constexpr int BAR_BYTES = ((1 + 6 * NST + 3 * NSB + (QT ? 1 : 0)) * 8 + 4 + 15) / 16 * 16;
+  // buffer, q_moved (Q in TMEM)
+  // then the TMEM address and 4 exact-P flag bytes per S buffer (one per
+  // softmax warp)
+  static constexpr int BAR_BYTES = ((1 + 6 * NST + 3 * NSB + (QT ? 1 : 0)) * 8 + 4 + 4 * NSB + 15) / 16 * 16;
   static constexpr int SMEM = 1024 + SMEM_DATA + BAR_BYTES;   // 1024: alignment slack for SW128
   static_assert(CPS * SMEM <= 232448, "shared memory for CPS CTAs per SM");
   static_assert(BN % 64 == 0, "P is stored 32 columns (64 keys) at a time");
@@ -273,14 +272,15 @@ __device__ __forceinline__ void dequant_tile(uint8_t* tile, float scale, int lan
   constexpr int UPR = T::RB8 / 16;         // 16-byte fp8 units per box row
   constexpr int U = T::NCC8 * UPR;         // units per key row
   const uint8_t* f8 = tile + T::F8_OFF;
+  const uint64_t scale2 = dequant_scale2(scale);
   auto out_unit = [&](int r, int d16, const uint4& w) {
     // 16 codes = dims [16 d16, 16 d16 + 16) -> two 16-byte bf16 units
     const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
     uint32_t o[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      o[2 * k] = dequant_e4m3x2(wv[k] & 0xffffu, scale);
-      o[2 * k + 1] = dequant_e4m3x2(wv[k] >> 16, scale);
+      o[2 * k] = dequant_e4m3x2<0>(wv[k], scale2);
+      o[2 * k + 1] = dequant_e4m3x2<1>(wv[k], scale2);
     }
     const int chunk = d16 >> 2;
     const int unit0 = (d16 & 3) * 2;
@@ -372,6 +372,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   uint64_t* o_done = p_full + T::NSB;
   uint64_t* q_moved = o_done + T::NSB;   // Q in TMEM: the softmax warps copied it (4 arrivals)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_moved + (T::QT ? 1 : 0));
+  uint8_t* vflag = reinterpret_cast<uint8_t*>(tmem_slot + 1);   // [NSB][4]: softmax warp wants exact P
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -524,8 +525,6 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     if (lane == 0) {
       constexpr uint32_t idesc_pv = idesc_bf16(kRows, D, false, true);
       const uint32_t v_ring = smem_u32(v_s);
-      const int pos_min = ctx + t0;
-      const int lo_max = p.window > 0 ? ctx + t_end - 1 - p.window + 1 : 0;
       bool ok = true;
       for (int jj = 0; jj < n && ok; ++jj) {
         const int st = jj % NST;
@@ -535,20 +534,24 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         tc_fence_after();
         const uint32_t tP = tbase + static_cast<uint32_t>(T::sbuf(jj) * BN);
         const uint32_t v_u = v_ring + st * T::TILE;
-        // P columns: k-step s (16 keys) at column 8s; on split tiles P_hi at
-        // 16s and P_lo at 16s + 8
-        const bool split = split_p_tile((kt0 + jj) * BN, BN, pos_min, lo_max, L, p.window);
-        const uint32_t pstep = split ? 16u : 8u;
+        // P columns: k-step s (16 keys): P_hi at 16s, P_lo at 16s + 8; the
+        // P_lo pass runs when a softmax warp flagged the tile (flags written
+        // before the warps arrived on p_full)
+        const uint32_t hot = *reinterpret_cast<volatile const uint32_t*>(vflag + 4 * T::sbuf(jj));
 #pragma unroll
         for (int s = 0; s < BN / 16; ++s) {
           const uint64_t bd = sdesc_sw128(v_u + s * 16 * 128, T::KV_CHUNK, 1024);
-          umma_ts(tbase + T::TMEM_O, tP + s * pstep, bd, idesc_pv, (jj > 0 || s > 0) ? 1u : 0u);
+          umma_ts(tbase + T::TMEM_O, tP + s * 16, bd, idesc_pv, (jj > 0 || s > 0) ? 1u : 0u);
         }
-        if (split) {
+        if (hot != 0u) {
+          // P_lo pass over the rows (TMEM lanes) of the warps that flagged the tile
+          uint32_t mask[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) mask[q] = ((hot >> (8 * q)) & 0xffu) ? 0u : 0xffffffffu;
 #pragma unroll
           for (int s = 0; s < BN / 16; ++s) {
             const uint64_t bd = sdesc_sw128(v_u + s * 16 * 128, T::KV_CHUNK, 1024);
-            umma_ts(tbase + T::TMEM_O, tP + s * 16 + 8, bd, idesc_pv, 1u);
+            umma_ts_masked(tbase + T::TMEM_O, tP + s * 16 + 8, bd, idesc_pv, 1u, mask);
           }
         }
         umma_commit(&o_done[T::sbuf(jj)]);
@@ -569,7 +572,6 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     const int lo = p.window > 0 ? pos - p.window + 1 : INT_MIN / 2;
     const bool capped = p.cap_log2 > 0.f;
     const bool plain = !capped && p.scale_log2 > 0.f;
-    const int lo_max_cta = p.window > 0 ? ctx + t_end - 1 - p.window + 1 : 0;
     const int l_pad = ((L + ps - 1) >> ps_log2) << ps_log2;   // end of the last page
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -610,7 +612,6 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       for (int c = 0; c < BN / 32; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       tmem_wait_ld();
       const bool full = (k0 >= lo) && (k0 + BN - 1 <= pos);
-      const bool split = split_p_tile(k0, BN, ctx + t0, lo_max_cta, L, p.window);
       float mx8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = -INFINITY;
@@ -645,50 +646,65 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       const float m_use = need ? m_new : m_run;
       const float m_base = (m_use == -INFINITY) ? 0.f : m_use;
       const float alpha = (m_use == m_run || m_use == -INFINITY) ? 1.f : ex2(m_run - m_use);
+      // Does some row of this warp take more than 1/kHotShare of its running
+      // denominator from one key of the tile?  Decided before the
+      // exponentials on a lower bound of the new denominator (the old one
+      // rescaled, plus the tile's largest weight pm, with mx in the
+      // exponent's units; -inf gives 0): a superset of such rows.
+      const float pm = ex2(mx - m_base);
+      const bool hot = __any_sync(0xffffffffu, row_ok && pm * (kHotShare - 1.f) > l_run * alpha);
       // exponentials with packed fp32x2 FFMA / FADD (moving part of them to a
       // polynomial on the FMA pipe was measured slower: issue-bound, not
-      // MUFU-bound).  P overwrites the score registers it consumes: P_hi of
-      // pair i in sr[i]; on split tiles each 16-key block b holds its 8 P_hi
-      // columns then its 8 P_lo columns in sr[16b .. 16b + 15].
+      // MUFU-bound).  P overwrites the score registers it consumes: each
+      // 16-key block b holds its 8 P_hi columns in sr[16b .. 16b + 7] and, in
+      // a hot warp, its 8 P_lo columns in sr[16b + 8 .. 16b + 15]; the PV
+      // issuer runs the P_lo pass with the rows of the other warps masked, so
+      // their stale columns there are never read into O.
       const float am = plain ? p.scale_log2 : 1.f;
       const float2 am2 = make_float2(am, am);
       const float2 nm2 = make_float2(-m_base, -m_base);
       float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      if (split) {
+      if (hot) {
 #pragma unroll
         for (int blk = 0; blk < BN / 16; ++blk) {
-          float2 e[8];
+          float2 ev[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int k = blk * 16 + 2 * i;
             const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), am2, nm2);
-            e[i] = make_float2(ex2(x.x), ex2(x.y));
-            ls2[i & 1] = __fadd2_rn(ls2[i & 1], e[i]);
+            ev[i] = make_float2(ex2(x.x), ex2(x.y));
+            ls2[i & 1] = __fadd2_rn(ls2[i & 1], ev[i]);
           }
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const uint32_t hi = pack_bf16x2(e[i].x, e[i].y);
+            const uint32_t hi = pack_bf16x2(ev[i].x, ev[i].y);
             sr[blk * 16 + i] = hi;
             sr[blk * 16 + 8 + i] =
-                pack_bf16x2(e[i].x - __uint_as_float(hi << 16), e[i].y - __uint_as_float(hi & 0xffff0000u));
+                pack_bf16x2(ev[i].x - __uint_as_float(hi << 16), ev[i].y - __uint_as_float(hi & 0xffff0000u));
           }
         }
       } else {
+        // in place: pair i of a block is written to slot i after slots 2i, 2i + 1 were read
 #pragma unroll
-        for (int i = 0; i < BN / 2; ++i) {
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), am2, nm2);
-          const float2 e = make_float2(ex2(x.x), ex2(x.y));
-          ls2[i & 1] = __fadd2_rn(ls2[i & 1], e);
-          sr[i] = pack_bf16x2(e.x, e.y);
+        for (int blk = 0; blk < BN / 16; ++blk) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int k = blk * 16 + 2 * i;
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), am2, nm2);
+            const float2 ev = make_float2(ex2(x.x), ex2(x.y));
+            ls2[i & 1] = __fadd2_rn(ls2[i & 1], ev);
+            sr[blk * 16 + i] = pack_bf16x2(ev.x, ev.y);
+          }
         }
       }
       const float2 lt = __fadd2_rn(ls2[0], ls2[1]);
       const float ls = lt.x + lt.y;
       l_run = l_run * alpha + ls;
       m_run = m_use;
+      if (lane == 0) vflag[4 * T::sbuf(j) + wq] = hot ? 1 : 0;   // read by the PV issuer after p_full
       static_assert(BN == 64, "P stores below assume 32-column halves");
       tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
-      if (split) tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));   // over S already read
+      tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));   // over S already read
       tmem_wait_st();
       if (any_need && j > 0) {
         // O must hold PV of tile j-1 before it is rescaled (and no PV may run meanwhile)
@@ -802,6 +818,7 @@ cudaError_t launch_ext(const CUtensorMap& tmq, const CUtensorMap& tmk, const CUt
   return cudaLaunchKernelEx(&cfg, kern, tmq, tmk, tmv, p);
 }
 
+
 // e4m3 cache, dequantised once per call: every page a request attends to is
 // written as bf16(float(code) * scale) into a dense copy, page i of request
 // b at copy page b * maxp + i, with an identity block table beside it; the
@@ -840,8 +857,8 @@ __global__ void __launch_bounds__(256) extend_kv_copy_kernel(const KvCopyParams 
   const int first = p.window > 0 ? max(0, ctx - p.window + 1) : 0;   // first key any query attends
   if ((i + 1) * ps <= first || i * ps >= L) return;
   const int src = p.block_table[static_cast<int64_t>(b) * p.bt_stride + i];
-  const float k_sc = p.k_scales != nullptr ? p.k_scales[b] : p.k_scale;
-  const float v_sc = p.v_scales != nullptr ? p.v_scales[b] : p.v_scale;
+  const uint64_t k_sc2 = dequant_scale2(p.k_scales != nullptr ? p.k_scales[b] : p.k_scale);
+  const uint64_t v_sc2 = dequant_scale2(p.v_scales != nullptr ? p.v_scales[b] : p.v_scale);
   constexpr int UPH = D / 16;   // 16-code units per head row
   const int units = ps * p.num_kv_heads * UPH;
   const int64_t page_elems = static_cast<int64_t>(ps) * p.num_kv_heads * D;
@@ -871,10 +888,10 @@ __global__ void __launch_bounds__(256) extend_kv_copy_kernel(const KvCopyParams 
     uint32_t ko[8], vo[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      ko[2 * k] = dequant_e4m3x2(ka[k] & 0xffffu, k_sc);
-      ko[2 * k + 1] = dequant_e4m3x2(ka[k] >> 16, k_sc);
-      vo[2 * k] = dequant_e4m3x2(va[k] & 0xffffu, v_sc);
-      vo[2 * k + 1] = dequant_e4m3x2(va[k] >> 16, v_sc);
+      ko[2 * k] = dequant_e4m3x2<0>(ka[k], k_sc2);
+      ko[2 * k + 1] = dequant_e4m3x2<1>(ka[k], k_sc2);
+      vo[2 * k] = dequant_e4m3x2<0>(va[k], v_sc2);
+      vo[2 * k + 1] = dequant_e4m3x2<1>(va[k], v_sc2);
     }
     kd[2 * u] = make_uint4(ko[0], ko[1], ko[2], ko[3]);
     kd[2 * u + 1] = make_uint4(ko[4], ko[5], ko[6], ko[7]);
