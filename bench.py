@@ -647,8 +647,9 @@ def cpu_baseline(p, ep, n_requests: int, min_seconds: float = 6.0):
     heads; all cores, repeated until about min_seconds have been timed, at
     least 3 passes), whole requests of the extend workload (all cores; the
     shortest requests in batch order until about a fifth of the workload's
-    FLOPs), and the tiny decode workload on one core.  ``value`` is the
-    decode figure, in the unit of the benchmark's metric."""
+    FLOPs), one pass over each other decode workload (all cores), and the
+    tiny decode workload on one core.  ``value`` is the decode figure, in
+    the unit of the benchmark's metric."""
     import oracle
     from paged_kv_gqa_12_gb300 import workloads as wl
     rows = np.arange(min(n_requests, p.batch), dtype=np.int32)
@@ -688,6 +689,15 @@ def cpu_baseline(p, ep, n_requests: int, min_seconds: float = 6.0):
                          "cores": cores, "kind": "oracle", "seconds": round(et, 3),
                          "sample": f"extend requests {chosen} of the extend workload (whole requests, all "
                                    f"{ep.num_q_heads} heads), {fl} algorithmic FLOPs ({fl / total:.1%} of the call)"}
+    # the other decode workloads: one pass over the whole batch each, all cores
+    for name in ("decode_e4m3_window", "decode_softcap_d256"):
+        op = wl.workload_problem(name)
+        t = time.perf_counter()
+        oracle.attention(op, num_threads=cores)
+        ot = time.perf_counter() - t
+        ob = decode_bytes(op)
+        res[name] = {"value": round(ob / ot / 1e12, 9), "unit": "TB/s", "cores": cores, "kind": "oracle",
+                     "seconds": round(ot, 3), "sample": f"the whole {name} batch ({ob} algorithmic bytes), one pass"}
     tp = wl.workload_problem("decode_tiny")
     passes, dt = 0, 0.0
     while passes < 3 or dt < 2.0:

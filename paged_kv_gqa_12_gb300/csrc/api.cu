@@ -241,7 +241,7 @@ using namespace pa;
 
 extern "C" {
 
-int32_t pa_version(void) { return 103; }
+int32_t pa_version(void) { return 104; }
 
 const char* pa_status_string(pa_status status) {
   switch (status) {
