@@ -534,14 +534,14 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         tc_fence_after();
         const uint32_t tP = tbase + static_cast<uint32_t>(T::sbuf(jj) * BN);
         const uint32_t v_u = v_ring + st * T::TILE;
-        // P columns: k-step s (16 keys): P_hi at 16s, P_lo at 16s + 8; the
+        // P columns: k-step s (16 keys): P_hi at 8s, P_lo at 32 + 8s; the
         // P_lo pass runs when a softmax warp flagged the tile (flags written
         // before the warps arrived on p_full)
         const uint32_t hot = *reinterpret_cast<volatile const uint32_t*>(vflag + 4 * T::sbuf(jj));
 #pragma unroll
         for (int s = 0; s < BN / 16; ++s) {
           const uint64_t bd = sdesc_sw128(v_u + s * 16 * 128, T::KV_CHUNK, 1024);
-          umma_ts(tbase + T::TMEM_O, tP + s * 16, bd, idesc_pv, (jj > 0 || s > 0) ? 1u : 0u);
+          umma_ts(tbase + T::TMEM_O, tP + s * 8, bd, idesc_pv, (jj > 0 || s > 0) ? 1u : 0u);
         }
         if (hot != 0u) {
           // P_lo pass over the rows (TMEM lanes) of the warps that flagged the tile
@@ -551,7 +551,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
 #pragma unroll
           for (int s = 0; s < BN / 16; ++s) {
             const uint64_t bd = sdesc_sw128(v_u + s * 16 * 128, T::KV_CHUNK, 1024);
-            umma_ts_masked(tbase + T::TMEM_O, tP + s * 16 + 8, bd, idesc_pv, 1u, mask);
+            umma_ts_masked(tbase + T::TMEM_O, tP + 32 + s * 8, bd, idesc_pv, 1u, mask);
           }
         }
         umma_commit(&o_done[T::sbuf(jj)]);
@@ -655,11 +655,11 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       const bool hot = __any_sync(0xffffffffu, row_ok && pm * (kHotShare - 1.f) > l_run * alpha);
       // exponentials with packed fp32x2 FFMA / FADD (moving part of them to a
       // polynomial on the FMA pipe was measured slower: issue-bound, not
-      // MUFU-bound).  P overwrites the score registers it consumes: each
-      // 16-key block b holds its 8 P_hi columns in sr[16b .. 16b + 7] and, in
-      // a hot warp, its 8 P_lo columns in sr[16b + 8 .. 16b + 15]; the PV
-      // issuer runs the P_lo pass with the rows of the other warps masked, so
-      // their stale columns there are never read into O.
+      // MUFU-bound).  P_hi of pair i overwrites score register i (the pairs
+      // read before it) and lands in TMEM column i; a hot warp also stores
+      // each 16-key block's 8 P_lo columns at 32 + 8 b as soon as they exist.
+      // The PV issuer runs the P_lo pass with the rows of the other warps
+      // masked, so their columns 32 .. 63 (old scores) are never read into O.
       const float am = plain ? p.scale_log2 : 1.f;
       const float2 am2 = make_float2(am, am);
       const float2 nm2 = make_float2(-m_base, -m_base);
@@ -675,26 +675,23 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
             ev[i] = make_float2(ex2(x.x), ex2(x.y));
             ls2[i & 1] = __fadd2_rn(ls2[i & 1], ev[i]);
           }
+          uint32_t lo[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const uint32_t hi = pack_bf16x2(ev[i].x, ev[i].y);
-            sr[blk * 16 + i] = hi;
-            sr[blk * 16 + 8 + i] =
-                pack_bf16x2(ev[i].x - __uint_as_float(hi << 16), ev[i].y - __uint_as_float(hi & 0xffff0000u));
+            sr[blk * 8 + i] = hi;   // registers 8 b .. 8 b + 7 were read by this block or an earlier one
+            lo[i] = pack_bf16x2(ev[i].x - __uint_as_float(hi << 16), ev[i].y - __uint_as_float(hi & 0xffff0000u));
           }
+          tmem_st8(tS + 32 + blk * 8, lo);
         }
       } else {
-        // in place: pair i of a block is written to slot i after slots 2i, 2i + 1 were read
+        // in place: pair i is written to register i after registers 2i, 2i + 1 were read
 #pragma unroll
-        for (int blk = 0; blk < BN / 16; ++blk) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int k = blk * 16 + 2 * i;
-            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), am2, nm2);
-            const float2 ev = make_float2(ex2(x.x), ex2(x.y));
-            ls2[i & 1] = __fadd2_rn(ls2[i & 1], ev);
-            sr[blk * 16 + i] = pack_bf16x2(ev.x, ev.y);
-          }
+        for (int i = 0; i < BN / 2; ++i) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), am2, nm2);
+          const float2 ev = make_float2(ex2(x.x), ex2(x.y));
+          ls2[i & 1] = __fadd2_rn(ls2[i & 1], ev);
+          sr[i] = pack_bf16x2(ev.x, ev.y);
         }
       }
       const float2 lt = __fadd2_rn(ls2[0], ls2[1]);
@@ -704,7 +701,6 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       if (lane == 0) vflag[4 * T::sbuf(j) + wq] = hot ? 1 : 0;   // read by the PV issuer after p_full
       static_assert(BN == 64, "P stores below assume 32-column halves");
       tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
-      tmem_st32(tS + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));   // over S already read
       tmem_wait_st();
       if (any_need && j > 0) {
         // O must hold PV of tile j-1 before it is rescaled (and no PV may run meanwhile)
