@@ -84,18 +84,33 @@ struct ExtendParams {
   uint16_t* out;
   int64_t out_stride_tok, out_stride_head;
   float* lse;
-  int2* work;
+  int4* work;               // [work_cap][2]: WorkItem
   int* work_count;
   int work_cap;
   uint32_t* err;
 };
 
+// A work item: query tile mt of request b, with the request's first query
+// row, query count and sequence length (read from the metadata once, by the
+// scheduler), 32 bytes.
+struct WorkItem {
+  int b, mt, qs, qlen, L, pad0, pad1, pad2;
+};
+static_assert(sizeof(WorkItem) == 32, "two 16-byte loads per item");
+
+__device__ __forceinline__ WorkItem load_item(const ExtendParams& p, int idx) {
+  const int4 a = p.work[2 * idx];
+  const int4 c = p.work[2 * idx + 1];
+  return WorkItem{a.x, a.y, a.z, a.w, c.x, 0, 0, 0};
+}
+
 // Key tiles an item touches (its cost), from the rows it holds.
-__device__ __forceinline__ bool item_range(const ExtendParams& p, int b, int mt, int& qs, int& qlen, int& ctx,
+__device__ __forceinline__ bool item_range(const ExtendParams& p, const WorkItem& it, int& qs, int& qlen, int& ctx,
                                            int& t0, int& t_end, int& lo_min, int& kt0, int& n_tiles) {
-  qs = p.qsl[b];
-  qlen = p.qsl[b + 1] - qs;
-  const int L = p.seq_lens[b];
+  qs = it.qs;
+  qlen = it.qlen;
+  const int L = it.L;
+  const int mt = it.mt;
   ctx = L - qlen;
   t0 = mt * p.tm;
   if (qlen <= 0 || ctx < 0 || L > p.max_kv || qs < 0 || qs + qlen > p.total_q || t0 >= qlen) return false;
@@ -183,7 +198,10 @@ __global__ void __launch_bounds__(kSchedThreads) extend_schedule_kernel(const Ex
     const int nmt = (qlen + p.tm - 1) / p.tm;
     for (int mt = lane; mt < nmt; mt += 32) {
       const int pos = atomicAdd(&s_off[min(tile_cost(L - qlen, qlen, mt, p.tm, p.window, p.block_n), kBuckets - 1)], 1);
-      if (pos < p.work_cap) p.work[pos] = make_int2(b, mt);
+      if (pos < p.work_cap) {
+        p.work[2 * pos] = make_int4(b, mt, qs, qlen);
+        p.work[2 * pos + 1] = make_int4(L, 0, 0, 0);
+      }
     }
   }
   if (tid == 0) {
@@ -333,17 +351,20 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     prefetch_tensormap(&tmv);
   }
   pdl_wait_primary();  // the scheduler's work list is complete and visible
-  if (idx >= *p.work_count) return;
+  // the count and this CTA's entry in one round trip (idx < the list's
+  // capacity: the entry is read only when idx < count)
+  const int count = *p.work_count;
+  const WorkItem item = load_item(p, idx);
+  if (idx >= count) return;
   // another CTA's wait already expired: leave (CTA-uniform, before any TMEM
   // allocation).  Other error bits (a bad request or page id) leave the rest
   // of the call running.
   if (__syncthreads_or(threadIdx.x == 0 &&
                        (*reinterpret_cast<volatile uint32_t*>(p.err) & kErrWaitTimeout) != 0u))
     return;
-  const int2 item = p.work[idx];
-  const int b = item.x;
+  const int b = item.b;
   int qs, qlen, ctx, t0, t_end, lo_min, kt0, n;
-  if (!item_range(p, b, item.y, qs, qlen, ctx, t0, t_end, lo_min, kt0, n)) return;
+  if (!item_range(p, item, qs, qlen, ctx, t0, t_end, lo_min, kt0, n)) return;
   const int L = ctx + qlen;
   const int G = p.group;
   const int ps = p.page_size;
@@ -378,6 +399,24 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   const int warp = tid >> 5;
   const int lane = tid & 31;
 
+  // page coordinate of this lane's page of key tile j (TMA producers); pages
+  // with no attended key are fetched out of bounds, where TMA writes zeros
+  // (and so are ids outside the pool, which are flagged: the rest of the
+  // call is unaffected)
+  const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
+  auto page_coord = [&](int j) {
+    const int pg = (((kt0 + j) * BN) >> ps_log2) + lane;
+    const bool outside = (pg * ps >= L) || ((pg + 1) * ps <= lo_min);
+    if (outside) return p.num_pages;
+    const int id = bt_row[pg];
+    if (static_cast<unsigned>(id) < static_cast<unsigned>(p.num_pages)) return id;
+    atomicOr(p.err, kErrPageId);
+    return p.num_pages;
+  };
+  // the producers read the first tile's page ids while the CTA sets up
+  const int npg = BN >> ps_log2;
+  const int coord0 = ((warp == 0 || warp == 2) && lane < npg) ? page_coord(0) : 0;
+
   if (warp == 1) tmem_alloc(tmem_slot, T::TMEM_COLS);
   if (tid == 0) {
     mbar_init(q_full, 1);
@@ -396,6 +435,10 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     }
     if (T::QT) mbar_init(q_moved, 4);
     fence_mbar_init();
+    // Q right away (the other threads wait on q_full after the barrier below)
+    mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(T::NCH * p.tm * G * 128));
+#pragma unroll
+    for (int c = 0; c < T::NCH; ++c) tma_load_3d(q_chunk(c), &tmq, c * 64, kvh * G, qs + t0, q_full);
   }
   tc_fence_before();
   __syncthreads();
@@ -403,33 +446,13 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   const uint32_t tbase = *tmem_slot;
 
   if (warp == 0 || warp == 2) {
-    // ---------------- TMA producers: warp 0 -> Q and the K ring, warp 2 -> the V ring ----------------
+    // ---------------- TMA producers: warp 0 -> the K ring (Q was issued above), warp 2 -> the V ring ----------------
     const bool is_k = warp == 0;
     const CUtensorMap* map = is_k ? &tmk : &tmv;
     uint64_t* full = is_k ? k_full : v_full;
     uint64_t* empty = is_k ? k_empty : v_empty;
     uint8_t* ring = is_k ? k_s : v_s;
-    const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.bt_stride;
     bool ok = true;
-    if (is_k && lane == 0) {
-      mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(T::NCH * p.tm * G * 128));
-#pragma unroll
-      for (int c = 0; c < T::NCH; ++c) tma_load_3d(q_chunk(c), &tmq, c * 64, kvh * G, qs + t0, q_full);
-    }
-    const int npg = BN >> ps_log2;
-    // page coordinate of this lane's page of key tile j; pages with no
-    // attended key are fetched out of bounds, where TMA writes zeros
-    // (and so are ids outside the pool, which are flagged: the rest of the
-    // call is unaffected)
-    auto page_coord = [&](int j) {
-      const int pg = (((kt0 + j) * BN) >> ps_log2) + lane;
-      const bool outside = (pg * ps >= L) || ((pg + 1) * ps <= lo_min);
-      if (outside) return p.num_pages;
-      const int id = bt_row[pg];
-      if (static_cast<unsigned>(id) < static_cast<unsigned>(p.num_pages)) return id;
-      atomicOr(p.err, kErrPageId);
-      return p.num_pages;
-    };
     if constexpr (!FP8) {
       for (int j = 0; j < n && ok; ++j) {
         const int stage = j % NST;
@@ -446,7 +469,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         if (lane == 0) mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(T::TILE));
         __syncwarp();
         if (lane < npg) {
-          const int coord = page_coord(j);
+          const int coord = j == 0 ? coord0 : page_coord(j);
           uint8_t* dst = ring + stage * T::TILE + lane * ps * 128;
 #pragma unroll
           for (int c = 0; c < T::NCH; ++c) tma_load_4d(dst + c * T::KV_CHUNK, map, c * 64, kvh, 0, coord, &full[stage]);
@@ -463,7 +486,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         if (lane == 0) mbar_arrive_expect_tx(&land[stage], static_cast<uint32_t>(BN * D));
         __syncwarp();
         if (lane < npg) {
-          const int coord = page_coord(j);
+          const int coord = j == 0 ? coord0 : page_coord(j);
           uint8_t* dst = ring + stage * T::TILE + T::F8_OFF + lane * ps * T::RB8;
 #pragma unroll
           for (int c = 0; c < T::NCC8; ++c)
@@ -759,6 +782,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       const float inv = (Z > 0.f) ? f / Z : 0.f;
       const int64_t orow = static_cast<int64_t>(qs + min(tok, qlen - 1));
       uint16_t* op = p.out + orow * p.out_stride_tok + static_cast<int64_t>(hq) * p.out_stride_head;
+      const bool row_a32 = (reinterpret_cast<uintptr_t>(op) & 31u) == 0;
       const uint32_t tO = tbase + lane_off + T::TMEM_O;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -766,15 +790,19 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         tmem_ld32(tO + c * 32, u);
         tmem_wait_ld();
         if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(op + c * 32);
+          uint32_t pk[16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(u[8 * v + 0]) * inv, __uint_as_float(u[8 * v + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(u[8 * v + 2]) * inv, __uint_as_float(u[8 * v + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(u[8 * v + 4]) * inv, __uint_as_float(u[8 * v + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(u[8 * v + 6]) * inv, __uint_as_float(u[8 * v + 7]) * inv);
-            dst[v] = w;
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+          uint16_t* dst = op + c * 32;
+          if (row_a32) {
+            // a whole 32-byte sector per lane: half the store instructions
+            st_global_v8(dst, pk);
+            st_global_v8(dst + 16, pk + 8);
+          } else {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           }
         }
       }
@@ -938,7 +966,7 @@ pa_status plan_extend(const pa_shape& s, int num_sms, pa_plan_t* out) {
   out->grid[0] = static_cast<int32_t>(work_cap * s.num_kv_heads);
   out->grid[1] = 1;
   out->grid[2] = 1;
-  out->scratch_bytes = kScratchHeaderBytes + align_up(work_cap * 8, 256);
+  out->scratch_bytes = kScratchHeaderBytes + align_up(work_cap * 32, 256);
   out->launches = 2;  // scheduler + attention kernel
   out->kv_copy = 0;
   if (s.kv_dtype == PA_KV_FP8_E4M3 && kv_copy_bytes(s) <= kMaxKvCopyBytes) {
@@ -1024,7 +1052,7 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
   int32_t pages = num_pages;
   if (copy) {
     const int64_t maxp = s.max_pages_per_seq;
-    uint8_t* cbase = sc + kScratchHeaderBytes + align_up(cap_items * 8, 256);
+    uint8_t* cbase = sc + kScratchHeaderBytes + align_up(cap_items * 32, 256);
     int32_t* bt_copy = reinterpret_cast<int32_t*>(cbase);
     uint8_t* kc = cbase + align_up(static_cast<int64_t>(s.max_batch) * maxp * 4, 256);
     uint8_t* vc = kc + align_up(kv_copy_bytes(s) / 2, 256);
@@ -1108,8 +1136,8 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
   p.lse = lse;
   p.err = reinterpret_cast<uint32_t*>(sc);
   p.work_count = reinterpret_cast<int*>(sc + 16);
-  p.work = reinterpret_cast<int2*>(sc + kScratchHeaderBytes);
-  p.work_cap = static_cast<int>((plan->scratch_bytes - kScratchHeaderBytes) / 8);
+  p.work = reinterpret_cast<int4*>(sc + kScratchHeaderBytes);
+  p.work_cap = static_cast<int>((plan->scratch_bytes - kScratchHeaderBytes) / 32);
   if (p.work_cap > cap_items) p.work_cap = static_cast<int>(cap_items);
 
   cudaError_t e;

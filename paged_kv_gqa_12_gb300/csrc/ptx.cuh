@@ -120,6 +120,13 @@ __device__ __forceinline__ bool poll_or_abort(uint64_t* bar, uint32_t parity, ui
   return true;
 }
 
+// One 32-byte global store (dst 32-byte aligned): a whole sector per lane.
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // ---- TMA ---------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,

@@ -143,26 +143,30 @@ def test_extend_fp8_identity_probe_bitwise():
         assert np.array_equal(out.astype(np.float64), ref_o), (Hq, Hkv, D, ps)
 
 
-def test_extend_fp8_copy_and_in_kernel_paths_agree():
+@pytest.mark.parametrize("D", [64, 128])
+def test_extend_fp8_copy_and_in_kernel_paths_agree(D):
     # the e4m3 cache reaches the attention kernel either as a bf16 copy made
     # once per call or dequantised per tile in shared memory: the same bf16
-    # values either way, so the outputs are bitwise equal
+    # values in the same key tiles either way, so the outputs are bitwise
+    # equal
     from paged_kv_gqa_12_gb300 import binding as pb
     for opts in ({}, {"window": 100, "sinks": True}):
-        p = _ext(71, Hq=32, Hkv=8, D=128, ps=16, ctx=CTX, ql=QL, kv_dtype="fp8_e4m3", k_scale=0.05,
+        p = _ext(71 + D, Hq=32, Hkv=8, D=D, ps=16, ctx=CTX, ql=QL, kv_dtype="fp8_e4m3", k_scale=0.05,
                  v_scale=0.07, **opts)
         d = gh.upload(p)
         copy_plan = gh.make_plan(p)
         assert copy_plan.kv_copy == 1
-        tile_plan = pb.plan(mode=pb.MODE_EXTEND, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+        tile_plan = pb.plan(mode=pb.MODE_EXTEND, num_q_heads=32, num_kv_heads=8, head_dim=D, page_size=16,
                             kv_dtype=pb.KV_FP8_E4M3, max_batch=p.batch, max_pages_per_seq=1 << 16,
                             max_total_q=p.num_rows, window=p.window, has_sinks=p.sinks is not None)
         assert tile_plan.kv_copy == 0
         o1, l1 = gh.run(p, d=d, plan=copy_plan)
         o2, l2 = gh.run(p, d=d, plan=tile_plan)
+        assert copy_plan.tile_tokens == tile_plan.tile_tokens
         assert np.array_equal(o1, o2) and np.array_equal(l1, l2), opts
         ref_o, ref_l = oracle.attention(p)
-        gh.assert_parity(o2, l2, ref_o, ref_l, what=f"extend fp8 in-kernel dequantisation {opts}")
+        gh.assert_parity(o1, l1, ref_o, ref_l, what=f"extend fp8 copy D={D} {opts}")
+        gh.assert_parity(o2, l2, ref_o, ref_l, what=f"extend fp8 in-kernel dequantisation D={D} {opts}")
 
 
 @pytest.mark.parametrize("opts", [{}, {"window": 4096, "sinks": True}])
