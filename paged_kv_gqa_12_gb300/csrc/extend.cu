@@ -271,11 +271,11 @@ struct ExtTraits {
   __device__ static __forceinline__ uint32_t sphase(int j) {
     return (static_cast<unsigned>(j) / static_cast<unsigned>(NSB)) & 1u;
   }
-  // mbarriers: q_full, six per ring stage, s_full/p_full/o_done per S
+  // mbarriers: q_full, six per ring stage, s_full/2 x p_half/o_done per S
   // buffer, q_moved (Q in TMEM)
   // then the TMEM address and 4 exact-P flag bytes per S buffer (one per
   // softmax warp)
-  static constexpr int BAR_BYTES = ((1 + 6 * NST + 3 * NSB + (QT ? 1 : 0)) * 8 + 4 + 4 * NSB + 15) / 16 * 16;
+  static constexpr int BAR_BYTES = ((1 + 6 * NST + 4 * NSB + (QT ? 1 : 0)) * 8 + 4 + 4 * NSB + 15) / 16 * 16;
   static constexpr int SMEM = 1024 + SMEM_DATA + BAR_BYTES;   // 1024: alignment slack for SW128
   static_assert(CPS * SMEM <= 232448, "shared memory for CPS CTAs per SM");
   static_assert(BN % 64 == 0, "P is stored 32 columns (64 keys) at a time");
@@ -389,8 +389,8 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
   uint64_t* k_land = v_empty + NST;   // fp8: the e4m3 tile has landed (before dequantisation)
   uint64_t* v_land = k_land + NST;
   uint64_t* s_full = v_land + NST;
-  uint64_t* p_full = s_full + T::NSB;
-  uint64_t* o_done = p_full + T::NSB;
+  uint64_t* p_half = s_full + T::NSB;      // [NSB][2]: a 32-key half of P stored (4 arrivals)
+  uint64_t* o_done = p_half + 2 * T::NSB;
   uint64_t* q_moved = o_done + T::NSB;   // Q in TMEM: the softmax warps copied it (4 arrivals)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_moved + (T::QT ? 1 : 0));
   uint8_t* vflag = reinterpret_cast<uint8_t*>(tmem_slot + 1);   // [NSB][4]: softmax warp wants exact P
@@ -430,7 +430,8 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
     }
     for (int i = 0; i < T::NSB; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&p_half[2 * i], 4);
+      mbar_init(&p_half[2 * i + 1], 4);
       mbar_init(&o_done[i], 1);
     }
     if (T::QT) mbar_init(q_moved, 4);
@@ -551,7 +552,7 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       bool ok = true;
       for (int jj = 0; jj < n && ok; ++jj) {
         const int st = jj % NST;
-        ok = poll_or_abort(&p_full[T::sbuf(jj)], T::sphase(jj), p.err) &&
+        ok = poll_or_abort(&p_half[2 * T::sbuf(jj)], T::sphase(jj), p.err) &&
              poll_or_abort(&v_full[st], (jj / NST) & 1, p.err);
         if (!ok) break;
         tc_fence_after();
@@ -559,13 +560,20 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         const uint32_t v_u = v_ring + st * T::TILE;
         // P columns: k-step s (16 keys): P_hi at 8s, P_lo at 32 + 8s; the
         // P_lo pass runs when a softmax warp flagged the tile (flags written
-        // before the warps arrived on p_full)
+        // before the warps released the first half of P).  Steps 0 and 1
+        // need only the first half.
         const uint32_t hot = *reinterpret_cast<volatile const uint32_t*>(vflag + 4 * T::sbuf(jj));
 #pragma unroll
         for (int s = 0; s < BN / 16; ++s) {
+          if (s == 2) {
+            ok = poll_or_abort(&p_half[2 * T::sbuf(jj) + 1], T::sphase(jj), p.err);
+            if (!ok) break;
+            tc_fence_after();
+          }
           const uint64_t bd = sdesc_sw128(v_u + s * 16 * 128, T::KV_CHUNK, 1024);
           umma_ts(tbase + T::TMEM_O, tP + s * 8, bd, idesc_pv, (jj > 0 || s > 0) ? 1u : 0u);
         }
+        if (!ok) break;
         if (hot != 0u) {
           // P_lo pass over the rows (TMEM lanes) of the warps that flagged the tile
           uint32_t mask[4];
@@ -676,74 +684,28 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
       // exponent's units; -inf gives 0): a superset of such rows.
       const float pm = ex2(mx - m_base);
       const bool hot = __any_sync(0xffffffffu, row_ok && pm * (kHotShare - 1.f) > l_run * alpha);
-      // exponentials with packed fp32x2 FFMA / FADD (moving part of them to a
-      // polynomial on the FMA pipe was measured slower: issue-bound, not
-      // MUFU-bound).  P_hi of pair i overwrites score register i (the pairs
-      // read before it) and lands in TMEM column i; a hot warp also stores
-      // each 16-key block's 8 P_lo columns at 32 + 8 b as soon as they exist.
-      // The PV issuer runs the P_lo pass with the rows of the other warps
-      // masked, so their columns 32 .. 63 (old scores) are never read into O.
-      const float am = plain ? p.scale_log2 : 1.f;
-      const float2 am2 = make_float2(am, am);
-      const float2 nm2 = make_float2(-m_base, -m_base);
-      float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      if (hot) {
-#pragma unroll
-        for (int blk = 0; blk < BN / 16; ++blk) {
-          float2 ev[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int k = blk * 16 + 2 * i;
-            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), am2, nm2);
-            ev[i] = make_float2(ex2(x.x), ex2(x.y));
-            ls2[i & 1] = __fadd2_rn(ls2[i & 1], ev[i]);
-          }
-          uint32_t lo[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t hi = pack_bf16x2(ev[i].x, ev[i].y);
-            sr[blk * 8 + i] = hi;   // registers 8 b .. 8 b + 7 were read by this block or an earlier one
-            lo[i] = pack_bf16x2(ev[i].x - __uint_as_float(hi << 16), ev[i].y - __uint_as_float(hi & 0xffff0000u));
-          }
-          tmem_st8(tS + 32 + blk * 8, lo);
-        }
-      } else {
-        // in place: pair i is written to register i after registers 2i, 2i + 1 were read
-#pragma unroll
-        for (int i = 0; i < BN / 2; ++i) {
-          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), am2, nm2);
-          const float2 ev = make_float2(ex2(x.x), ex2(x.y));
-          ls2[i & 1] = __fadd2_rn(ls2[i & 1], ev);
-          sr[i] = pack_bf16x2(ev.x, ev.y);
-        }
-      }
-      const float2 lt = __fadd2_rn(ls2[0], ls2[1]);
-      const float ls = lt.x + lt.y;
-      l_run = l_run * alpha + ls;
-      m_run = m_use;
-      if (lane == 0) vflag[4 * T::sbuf(j) + wq] = hot ? 1 : 0;   // read by the PV issuer after p_full
-      static_assert(BN == 64, "P stores below assume 32-column halves");
-      tmem_st32(tS, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
-      tmem_wait_st();
+      // O is rescaled and value rows past the sequence end are zeroed before
+      // any P is released: PV of this tile may start on its first half
       if (any_need && j > 0) {
         // O must hold PV of tile j-1 before it is rescaled (and no PV may run meanwhile)
         ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[T::sbuf(j - 1)], T::sphase(j - 1), p.err));
         if (!ok) break;
         tc_fence_after();
         const uint32_t tO = tbase + lane_off + T::TMEM_O;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tO + c * 32, u);
+        // 16 columns at a time: the tile's 64 scores are live here
+#pragma unroll 1
+        for (int c = 0; c < D / 16; ++c) {
+          uint32_t u[16];
+          tmem_ld16(tO + c * 16, u);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
+          for (int i = 0; i < 16; i += 2) {
             const float2 v = __fmul2_rn(make_float2(__uint_as_float(u[i]), __uint_as_float(u[i + 1])),
                                         make_float2(alpha, alpha));
             u[i] = __float_as_uint(v.x);
             u[i + 1] = __float_as_uint(v.y);
           }
-          tmem_st32(tO + c * 32, u);
+          tmem_st16(tO + c * 16, u);
         }
         tmem_wait_st();
       }
@@ -763,9 +725,66 @@ extend_attn_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constan
         }
         fence_proxy_async_smem();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[T::sbuf(j)]);
+      if (lane == 0) vflag[4 * T::sbuf(j) + wq] = hot ? 1 : 0;   // read by the PV issuer after p_half
+      // exponentials with packed fp32x2 FFMA / FADD (moving part of them to a
+      // polynomial on the FMA pipe was measured slower: issue-bound, not
+      // MUFU-bound).  P_hi of pair i overwrites score register i (the pairs
+      // read before it) and lands in TMEM column i; a hot warp also stores
+      // each 16-key block's 8 P_lo columns at 32 + 8 b as soon as they exist.
+      // The PV issuer runs the P_lo pass with the rows of the other warps
+      // masked, so their columns 32 .. 63 (old scores) are never read into O.
+      // Each 32-key half of P is released on its own barrier as soon as it
+      // is stored, so the first two PV MMAs overlap the second half's
+      // exponentials.
+      static_assert(BN == 64, "P is released in two 32-key halves of 16 columns");
+      const float am = plain ? p.scale_log2 : 1.f;
+      const float2 am2 = make_float2(am, am);
+      const float2 nm2 = make_float2(-m_base, -m_base);
+      float2 ls2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      auto release = [&](int half) {
+        tmem_st16(tS + 16 * half, *reinterpret_cast<const uint32_t(*)[16]>(&sr[16 * half]));
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_half[2 * T::sbuf(j) + half]);
+      };
+      if (hot) {
+#pragma unroll
+        for (int blk = 0; blk < BN / 16; ++blk) {
+          float2 ev[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int k = blk * 16 + 2 * i;
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), am2, nm2);
+            ev[i] = make_float2(ex2(x.x), ex2(x.y));
+            ls2[i & 1] = __fadd2_rn(ls2[i & 1], ev[i]);
+          }
+          uint32_t lo[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t hi = pack_bf16x2(ev[i].x, ev[i].y);
+            sr[blk * 8 + i] = hi;   // registers 8 b .. 8 b + 7 were read by this block or an earlier one
+            lo[i] = pack_bf16x2(ev[i].x - __uint_as_float(hi << 16), ev[i].y - __uint_as_float(hi & 0xffff0000u));
+          }
+          tmem_st8(tS + 32 + blk * 8, lo);
+          if (blk == 1) release(0);
+        }
+      } else {
+        // in place: pair i is written to register i after registers 2i, 2i + 1 were read
+#pragma unroll
+        for (int i = 0; i < BN / 2; ++i) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), am2, nm2);
+          const float2 ev = make_float2(ex2(x.x), ex2(x.y));
+          ls2[i & 1] = __fadd2_rn(ls2[i & 1], ev);
+          sr[i] = pack_bf16x2(ev.x, ev.y);
+          if (i == 15) release(0);
+        }
+      }
+      release(1);
+      const float2 lt = __fadd2_rn(ls2[0], ls2[1]);
+      const float ls = lt.x + lt.y;
+      l_run = l_run * alpha + ls;
+      m_run = m_use;
     }
     if (ok && n > 0)
       ok = __all_sync(0xffffffffu, wait_or_abort(&o_done[T::sbuf(n - 1)], T::sphase(n - 1), p.err));
