@@ -691,6 +691,49 @@ def measure_extras(pb, wl, dp, dd, dev, stream):
                      "ms_write_only_flush": round(ms_write_only, 4),
                      "device_error": pb.check(scr)}
         del g, scr, out, lse
+    # extend at other head dims / group sizes on the extend workload's
+    # lengths (same flush, median of 30): the kernel configurations the
+    # benchmark step does not launch
+    base = wl.workload_problem("prefill")
+    ql = np.diff(base.query_start_loc)
+    for (Hq, Hkv, D) in ((32, 8, 64), (16, 8, 256), (64, 8, 128)):
+        p = wl.build_problem("extend", num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=16,
+                             seq_lens=base.seq_lens, query_lens=ql, seed=1004, poison=False)
+
+        def t8(a):
+            if a.dtype == np.uint16:
+                return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+            return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        g = {k: t8(getattr(p, a)) for k, a in (("q", "q"), ("k", "k_cache"), ("v", "v_cache"), ("bt", "block_table"),
+                                              ("sl", "seq_lens"), ("qsl", "query_start_loc"))}
+        plan = pb.plan(mode=pb.MODE_EXTEND, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=16,
+                       max_batch=p.batch, max_pages_per_seq=p.block_table.shape[1], max_total_q=p.num_rows)
+        scr = pb.alloc_scratch(plan, dev)
+        out = torch.empty(p.q.shape, dtype=torch.bfloat16, device=dev)
+
+        def call():
+            pb.extend(plan, g["q"], g["k"], g["v"], g["bt"], g["sl"], g["qsl"], scale=p.scale, out=out, scratch=scr,
+                      stream=stream)
+        for _ in range(5):
+            call()
+        ms = []
+        for i in range(30):
+            flush.fill_(i & 255)
+            flush_rd.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        t = statistics.median(ms) / 1e3
+        fl = extend_flops(p)
+        res[f"extend_hq{Hq}_hkv{Hkv}_d{D}"] = {
+            "workload": f"extend workload's lengths, Hq {Hq}, Hkv {Hkv}, D {D}, page 16, bf16",
+            "ms": round(t * 1e3, 4), "tflops": round(fl / t / 1e12, 2),
+            "frac_of_bf16_peak": round(fl / t / 1e12 / float(peaks.get("bf16_tflops", 1900.0)), 4),
+            "timing": "median of 30 calls; L2 flushed before each as above", "device_error": pb.check(scr)}
+        del g, scr, out
     return res
 
 
