@@ -532,9 +532,10 @@ def e2e_pipelined(torch, stream, copy_streams, host_in, dev_in, compute, dev_out
     inputs have landed, and copies dev_out[slot] back into host_out[slot] on
     the second copy stream once it is done.  So the inputs of step k+1 go in
     while step k computes and its results come back meanwhile, both
-    directions at once.  A slot is reused only after the step that used it
-    two steps before has been copied back.  The CUDA events bracket all of
-    it: the first input copy to the last result copy."""
+    directions at once.  A slot's inputs are overwritten once the step that
+    used them two steps before has computed, its outputs once that step's
+    results have been copied back.  The CUDA events bracket all of it: the
+    first input copy to the last result copy."""
     h2d, d2h = copy_streams
     in_ready = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
@@ -545,7 +546,7 @@ def e2e_pipelined(torch, stream, copy_streams, host_in, dev_in, compute, dev_out
         i = k % 2
         with torch.cuda.stream(h2d):
             if k >= 2:
-                h2d.wait_event(freed[i])
+                h2d.wait_event(done[i])   # step k - 2 has read its inputs
             for d, h in zip(dev_in[i], host_in):
                 d.copy_(h, non_blocking=True)
             in_ready[i].record(h2d)
@@ -556,6 +557,8 @@ def e2e_pipelined(torch, stream, copy_streams, host_in, dev_in, compute, dev_out
     for k in range(steps):
         i = k % 2
         stream.wait_event(in_ready[i])
+        if k >= 2:
+            stream.wait_event(freed[i])   # step k - 2's results are back on the host
         with torch.cuda.stream(stream):
             compute(dev_in[i], dev_out[i])
         done[i].record(stream)
