@@ -966,6 +966,23 @@ ExtChoice ext_choice(int D) {
 
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
+// Work items (query tiles) a plan has room for: every request's last tile
+// may be partial.
+int64_t work_capacity(const pa_shape& s) {
+  const int tm = kRows / (s.num_q_heads / s.num_kv_heads);
+  return (static_cast<int64_t>(s.max_total_q) + tm - 1) / tm + s.max_batch;
+}
+
+// Scratch an extend plan lays out: the header, the work list and, with an
+// e4m3 copy, the identity block table and the bf16 K and V copies.
+int64_t extend_scratch_bytes(const pa_shape& s, bool copy) {
+  int64_t b = kScratchHeaderBytes + align_up(work_capacity(s) * 32, 256);
+  if (copy)
+    b += align_up(static_cast<int64_t>(s.max_batch) * s.max_pages_per_seq * 4, 256) +
+         2 * align_up(kv_copy_bytes(s) / 2, 256);
+  return b;
+}
+
 }  // namespace
 
 pa_status plan_extend(const pa_shape& s, int num_sms, pa_plan_t* out) {
@@ -973,7 +990,7 @@ pa_status plan_extend(const pa_shape& s, int num_sms, pa_plan_t* out) {
   const int G = s.num_q_heads / s.num_kv_heads;
   const int tm = kRows / G;
   const ExtChoice ch = ext_choice(s.head_dim);
-  const int64_t work_cap = (static_cast<int64_t>(s.max_total_q) + tm - 1) / tm + s.max_batch;
+  const int64_t work_cap = work_capacity(s);
   if (work_cap * s.num_kv_heads > INT32_MAX) return PA_ERR_UNSUPPORTED;
   out->tile_tokens = ch.block_n;
   out->split_tiles = tm;
@@ -985,16 +1002,9 @@ pa_status plan_extend(const pa_shape& s, int num_sms, pa_plan_t* out) {
   out->grid[0] = static_cast<int32_t>(work_cap * s.num_kv_heads);
   out->grid[1] = 1;
   out->grid[2] = 1;
-  out->scratch_bytes = kScratchHeaderBytes + align_up(work_cap * 32, 256);
-  out->launches = 2;  // scheduler + attention kernel
-  out->kv_copy = 0;
-  if (s.kv_dtype == PA_KV_FP8_E4M3 && kv_copy_bytes(s) <= kMaxKvCopyBytes) {
-    // identity block table, then the bf16 K and V copies
-    out->kv_copy = 1;
-    out->scratch_bytes += align_up(static_cast<int64_t>(s.max_batch) * s.max_pages_per_seq * 4, 256) +
-                          2 * align_up(kv_copy_bytes(s) / 2, 256);
-    out->launches = 3;
-  }
+  out->kv_copy = (s.kv_dtype == PA_KV_FP8_E4M3 && kv_copy_bytes(s) <= kMaxKvCopyBytes) ? 1 : 0;
+  out->scratch_bytes = extend_scratch_bytes(s, out->kv_copy != 0);
+  out->launches = out->kv_copy ? 3 : 2;  // (e4m3 copy,) scheduler, attention kernel
   return PA_OK;
 }
 
@@ -1038,6 +1048,11 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
   if ((sinks != nullptr) != (s.has_sinks != 0)) return PA_ERR_INVALID_ARG;
   if (!scratch) return PA_ERR_INVALID_ARG;
   if (scratch_bytes < plan->scratch_bytes) return PA_ERR_SCRATCH_TOO_SMALL;
+  // the work list (and an e4m3 copy) are laid out from the shape's
+  // capacities: a plan edited by hand must still match them and leave room
+  const int64_t cap_items = work_capacity(s);
+  if (plan->grid[0] != cap_items * s.num_kv_heads) return PA_ERR_INVALID_ARG;
+  if (scratch_bytes < extend_scratch_bytes(s, fp8 && plan->kv_copy != 0)) return PA_ERR_SCRATCH_TOO_SMALL;
   if ((reinterpret_cast<uintptr_t>(scratch) & 255u) != 0) return PA_ERR_UNSUPPORTED;
   if (batch == 0 || total_q == 0) return PA_OK;
   if (!q || !out || !block_table || !seq_lens || !query_start_loc || bt_stride < 0) return PA_ERR_INVALID_ARG;
@@ -1060,7 +1075,6 @@ extern "C" pa_status pa_extend(const pa_plan_t* plan, const void* q, int64_t q_s
     return st;
   uint8_t* sc = static_cast<uint8_t*>(scratch);
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
-  const int64_t cap_items = plan->grid[0] / s.num_kv_heads;
   // e4m3 cache with a copy plan: dequantise the attended pages once into the
   // scratch workspace (after the work list), then attend over the bf16 copy
   const bool copy = fp8 && plan->kv_copy != 0 && batch <= 65535;

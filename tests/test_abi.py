@@ -161,6 +161,38 @@ def test_decode_rejects_hand_edited_plans(lib):
     assert _decode_args(tile) == pb.PA_ERR_INVALID_ARG
 
 
+def _extend_args(plan, sbytes=None, batch=4, total_q=64):
+    L = pb.load()
+    vp = ctypes.c_void_p
+    return L.pa_extend(ctypes.byref(plan), vp(0x10000), 32 * 128, 128, vp(0x20000), vp(0x40000), 16 * 8 * 128,
+                       8 * 128, 128, 100, vp(0x50000), 512, vp(0x60000), vp(0x68000), batch, total_q, 0.088, None,
+                       1.0, 1.0, None, None, vp(0x70000), 32 * 128, 128, None, vp(0x100000),
+                       plan.scratch_bytes if sbytes is None else sbytes, None)
+
+
+def test_extend_rejects_hand_edited_plans(lib):
+    # the work list (and an e4m3 copy) are laid out from the shape's
+    # capacities: a plan whose grid or scratch size no longer matches them
+    # is refused before anything is enqueued
+    try:
+        base = _plan(mode=pb.MODE_EXTEND, max_total_q=1024, max_batch=8)
+    except pb.PaError:
+        pytest.skip("extend planning unavailable")
+    grid = _plan(mode=pb.MODE_EXTEND, max_total_q=1024, max_batch=8)
+    grid.grid[0] += 8
+    assert _extend_args(grid) == pb.PA_ERR_INVALID_ARG
+    fp8 = _plan(mode=pb.MODE_EXTEND, max_total_q=1024, max_batch=8, kv_dtype=pb.KV_FP8_E4M3)
+    assert fp8.kv_copy == 1
+    full = fp8.scratch_bytes
+    fp8.scratch_bytes = base.scratch_bytes   # the copy's room edited away
+    assert _extend_args(fp8, sbytes=base.scratch_bytes) == pb.PA_ERR_SCRATCH_TOO_SMALL
+    assert _extend_args(fp8, sbytes=full - 256) == pb.PA_ERR_SCRATCH_TOO_SMALL
+    # the unedited plans pass these checks (empty calls: nothing to launch)
+    assert _extend_args(base, batch=0, total_q=0) == pb.PA_OK
+    fp8.scratch_bytes = full
+    assert _extend_args(fp8, batch=0, total_q=0) == pb.PA_OK
+
+
 def test_decode_empty_batch_is_noop(lib):
     plan = _plan()
     assert _decode_args(plan, batch=0) == pb.PA_OK
