@@ -255,7 +255,8 @@ struct ExtTraits {
   static constexpr int F8_OFF = TILE / 2;
   static constexpr uint32_t TMEM_COLS = 512 / CPS;   // CPS CTAs share an SM's 512 columns
   // S buffers: as many as the columns left beside O hold (2 for head_dim
-  // 128, 3 for 64, 4 for 256 with one CTA per SM); QK runs up to NSB - 1
+  // 128, 3 for 64, 3 for 256 with one CTA per SM and half of Q in TMEM, 4
+  // for its e4m3 form); QK runs up to NSB - 1
   // tiles ahead of the softmax
   static constexpr int Q_COLS = Q_TM_CH * 32;       // Q in TMEM: bf16 pairs, 32 columns per chunk
   static constexpr int NSB = (static_cast<int>(TMEM_COLS) - D - Q_COLS) / BN;
