@@ -237,7 +237,11 @@ pa_status pa_decode_static_scratch(const pa_plan_t* plan,
  * the call first writes bf16(float(code) * scale) of every page a request
  * reads into the scratch workspace (pages before the sliding window are
  * skipped) and attends over that copy; the values the attention sees are the
- * same either way.  Other arguments as for pa_decode. */
+ * same either way.  The work list and the copy are laid out from the plan's
+ * shape: a plan whose grid no longer matches that shape returns
+ * PA_ERR_INVALID_ARG, and a scratch smaller than the layout (the copy
+ * included) PA_ERR_SCRATCH_TOO_SMALL, before anything is enqueued.  Other
+ * arguments as for pa_decode. */
 pa_status pa_extend(const pa_plan_t* plan,
                     const void* q, int64_t q_stride_tok, int64_t q_stride_head,
                     const void* k_cache, const void* v_cache,
