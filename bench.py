@@ -737,6 +737,77 @@ def measure_extras(pb, wl, dp, dd, dev, stream):
             "frac_of_bf16_peak": round(fl / t / 1e12 / float(peaks.get("bf16_tflops", 1900.0)), 4),
             "timing": "median of 30 calls; L2 flushed before each as above", "device_error": pb.check(scr)}
         del g, scr, out
+    # KV append: the extend workload's new tokens written into their slots of
+    # a cache shaped like the workload's (bf16 copy; e4m3 quantisation into an
+    # e4m3 cache).  Bytes: the new K and V read, the slot mapping, the rows
+    # written; HBM-bound.
+    T, Hkv, D = base.num_rows, base.num_kv_heads, base.head_dim
+    ps = base.page_size
+    slots = np.empty(T, np.int64)
+    for b in range(base.batch):
+        q0, q1 = int(base.query_start_loc[b]), int(base.query_start_loc[b + 1])
+        L = int(base.seq_lens[b])
+        pos = np.arange(L - (q1 - q0), L)
+        slots[q0:q1] = base.block_table[b, pos // ps].astype(np.int64) * ps + pos % ps
+    g2 = torch.Generator(device="cpu").manual_seed(4243)
+    kn = torch.randn(T, Hkv, D, generator=g2).to(torch.bfloat16).to(dev)
+    vn = torch.randn(T, Hkv, D, generator=g2).to(torch.bfloat16).to(dev)
+    slot_t = torch.from_numpy(slots).to(dev)
+    for name, kvd, cdt, esz in (("append_bf16", pb.KV_BF16, torch.bfloat16, 2),
+                                ("append_e4m3", pb.KV_FP8_E4M3, torch.uint8, 1)):
+        kc = torch.zeros(base.k_cache.shape, dtype=cdt, device=dev)
+        vc = torch.zeros(base.v_cache.shape, dtype=cdt, device=dev)
+        ascr = torch.zeros(65536, dtype=torch.uint8, device=dev)
+
+        def call():
+            pb.append_kv(kn, vn, kc, vc, slot_t, kv_dtype=kvd, k_scale=0.05, v_scale=0.05, scratch=ascr,
+                         stream=stream)
+        for _ in range(5):
+            call()
+        ms = []
+        for i in range(30):
+            flush.fill_(i & 255)
+            flush_rd.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        t = statistics.median(ms) / 1e3
+        nb = T * Hkv * D * (2 * 2 + 2 * esz) + T * 8
+        res[name] = {"workload": f"the extend workload's {T} new tokens x {Hkv} kv heads x {D} dims into their "
+                                 f"slots ({'bf16' if esz == 2 else 'e4m3'} cache)",
+                     "ms": round(t * 1e3, 4), "gbs": round(nb / t / 1e9, 1),
+                     "frac_of_hbm": round(nb / t / 1e9 / peak_hbm, 4), "algorithmic_bytes": nb,
+                     "timing": "median of 30 calls; L2 flushed before each as above",
+                     "device_error": pb.check(ascr)}
+        del kc, vc
+    # CUDA-graph replay: the decode call with a capacity plan (no host
+    # lengths), captured once and replayed (inputs > L2, no flush)
+    gplan = pb.plan(**decode_plan_kw(pb, dp, "decode_llama3_8b"))
+    gscr = pb.alloc_scratch(gplan, dev)
+    gout = torch.empty(dp.q.shape, dtype=torch.bfloat16, device=dev)
+    glse = torch.empty(dp.q.shape[:2], dtype=torch.float32, device=dev)
+
+    def gcall():
+        pb.decode(gplan, dd["q"], dd["k"], dd["v"], dd["bt"], dd["sl"], scale=dp.scale, out=gout, lse=glse,
+                  sinks=dd["sinks"], k_scale=dp.k_scale, v_scale=dp.v_scale, scratch=gscr)
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        gcall()
+    torch.cuda.current_stream().wait_stream(cs)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        gcall()
+    t = _time_calls(torch, graph.replay, torch.cuda.current_stream())
+    nb = decode_bytes(dp)
+    res["decode_graph_replay"] = {"workload": "the decode workload through a captured CUDA graph (capacity plan)",
+                                  "ms": round(t * 1e3, 4), "kv_read_tbs": round(nb / t / 1e12, 4),
+                                  "frac_of_hbm": round(nb / t / 1e9 / peak_hbm, 4),
+                                  "max_splits": int(gplan.max_splits), "device_error": pb.check(gscr)}
     return res
 
 
