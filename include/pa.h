@@ -268,6 +268,8 @@ pa_status pa_extend(const pa_plan_t* plan,
  *                  e4m3(x / scale) (round to nearest even, saturated to +-448)
  *   scratch        optional (may be NULL): a scratch buffer whose error header
  *                  records slots outside the pool (those tokens are not written)
+ * One call moves fewer than 2^31 eight-element vectors (num_tokens * Hkv *
+ * head_dim / 8), else PA_ERR_UNSUPPORTED.
  * Asynchronous on `stream`; one kernel launch. */
 pa_status pa_append_kv(const void* k_new, const void* v_new, int64_t new_stride_tok, int64_t new_stride_head,
                        void* k_cache, void* v_cache,

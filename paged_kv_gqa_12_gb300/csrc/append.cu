@@ -30,25 +30,36 @@ struct AppendParams {
   uint8_t* v_cache;
   int64_t stride_page, stride_tok, stride_head;   // bytes
   int num_pages, page_size, num_kv_heads, head_dim, num_tokens;
+  int vpr_log2;        // log2(head_dim / 8): 8-element vectors per row
+  int ps_log2;         // log2(page_size) when it is a power of two, else -1
   const int64_t* slot_mapping;
   float k_scale, v_scale;
   uint32_t* err;   // optional error word
 };
 
+// (the host guarantees tokens x heads x head_dim / 8 < 2^31, so the thread
+// index and its row split stay in 32 bits; head_dim / 8 is a power of two)
 template <bool FP8>
 __global__ void __launch_bounds__(256) append_kv_kernel(const AppendParams p) {
-  const int vec_per_row = p.head_dim / 8;
-  const int64_t total = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads * vec_per_row;
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const uint32_t total = static_cast<uint32_t>(p.num_tokens) * static_cast<uint32_t>(p.num_kv_heads)
+                         << p.vpr_log2;
+  const uint32_t idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= total) return;
-  const int vv = static_cast<int>(idx % vec_per_row);
-  const int64_t th = idx / vec_per_row;
-  const int h = static_cast<int>(th % p.num_kv_heads);
-  const int t = static_cast<int>(th / p.num_kv_heads);
+  const int vv = static_cast<int>(idx & ((1u << p.vpr_log2) - 1u));
+  const uint32_t th = idx >> p.vpr_log2;
+  const uint32_t nh = static_cast<uint32_t>(p.num_kv_heads);
+  const int t = static_cast<int>(th / nh);
+  const int h = static_cast<int>(th - static_cast<uint32_t>(t) * nh);
   const int64_t slot = p.slot_mapping[t];
   if (slot < 0) return;                                   // padding token
-  const int64_t page = slot / p.page_size;
-  const int64_t off = slot - page * p.page_size;
+  int64_t page, off;
+  if (p.ps_log2 >= 0) {
+    page = slot >> p.ps_log2;
+    off = slot & ((int64_t{1} << p.ps_log2) - 1);
+  } else {
+    page = slot / p.page_size;
+    off = slot - page * p.page_size;
+  }
   if (page >= p.num_pages) {                              // outside the pool: nothing written
     if (p.err != nullptr && vv == 0 && h == 0) atomicOr(p.err, kErrPageId);
     return;
@@ -119,11 +130,14 @@ extern "C" pa_status pa_append_kv(const void* k_new, const void* v_new, int64_t 
   p.num_kv_heads = num_kv_heads;
   p.head_dim = head_dim;
   p.num_tokens = num_tokens;
+  p.vpr_log2 = head_dim == 64 ? 3 : (head_dim == 128 ? 4 : 5);
+  p.ps_log2 = (page_size & (page_size - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(page_size)) : -1;
   p.slot_mapping = slot_mapping;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
   p.err = static_cast<uint32_t*>(scratch);
   const int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * (head_dim / 8);
+  if (total >= (int64_t{1} << 31)) return PA_ERR_UNSUPPORTED;   // one call moves < 2^31 vectors
   const unsigned blocks = static_cast<unsigned>((total + 255) / 256);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (fp8) {
