@@ -169,6 +169,29 @@ def test_extend_fp8_copy_and_in_kernel_paths_agree(D):
         gh.assert_parity(o2, l2, ref_o, ref_l, what=f"extend fp8 in-kernel dequantisation D={D} {opts}")
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_extend_padded_output_rows(D):
+    # output rows 16 elements longer than head_dim: every other (token, head)
+    # row starts off a 32-byte boundary, so the epilogue takes its 16-byte
+    # stores there and its 32-byte stores elsewhere; the padding stays as set
+    import torch
+    from paged_kv_gqa_12_gb300 import binding as pb
+    p = _ext(211 + D, Hq=16, Hkv=4, D=D, ps=16, ctx=CTX, ql=QL, sinks=True)
+    d = gh.upload(p)
+    plan = gh.make_plan(p)
+    T, Hq = p.q.shape[0], p.q.shape[1]
+    full = torch.full((T, Hq, D + 8), 3.0, dtype=torch.bfloat16, device="cuda")
+    out = full.narrow(2, 0, D)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device="cuda")
+    scratch = pb.alloc_scratch(plan)
+    pb.extend(plan, d["q"], d["k"], d["v"], d["bt"], d["sl"], d["qsl"], scale=p.scale, out=out, lse=lse,
+              sinks=d["sinks"], scratch=scratch)
+    assert pb.check(scratch) == 0
+    ref_o, ref_l = oracle.attention(p)
+    gh.assert_parity(out.float().cpu().numpy(), lse.cpu().numpy(), ref_o, ref_l, what=f"extend padded rows D={D}")
+    assert bool((full[:, :, D:] == 3.0).all())
+
+
 @pytest.mark.parametrize("opts", [{}, {"window": 4096, "sinks": True}])
 def test_extend_long_context_sampled(opts):
     # contexts of 20-32K keys: work items of several hundred key tiles; the
