@@ -26,7 +26,9 @@
 //     overlaps this tile's softmax (a buffer is reused once the PV that read
 //     its P has completed); P (bf16) is written back
 //     over S and consumed from TMEM by O += P V (V read MN-major from shared
-//     memory); O stays in TMEM for the whole key loop.
+//     memory); O stays in TMEM for the whole key loop.  The softmax releases
+//     P in two 32-key halves on separate barriers, so PV starts on the first
+//     half while the second half's exponentials run.
 //   * head_dim 256 (one CTA per SM): the first half of Q's dims also lives
 //     in TMEM, copied there by the softmax warps from its TMA staging area in
 //     the last K ring stage, so half of QK's K steps read only K from shared
@@ -39,7 +41,8 @@
 //     out-of-bounds TMA boxes (zero fill), and value rows past the sequence end
 //     inside the last page are zeroed, so stale or NaN slots never meet P = 0.
 //   * A one-CTA scheduler kernel builds the (request, query tile) list from
-//     the device metadata, heaviest first; CTA i takes item i / Hkv.
+//     the device metadata, heaviest first, each entry carrying the request's
+//     query start, query count and length; CTA i takes item i / Hkv.
 //   * e4m3 cache: a call first writes bf16(float(code) * scale) of every
 //     attended page into a copy in the scratch workspace
 //     (extend_kv_copy_kernel) and this kernel reads the copy; plans whose
